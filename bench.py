@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark: draft-node verifications/s for GDN tree verify + commit on B300.
+
+One step = one pass of the whole hot path over one layer's batch: gdn_tree_verify (all
+nodes, all heads) followed by gdn_tree_commit (accepted paths), both through the C ABI.
+
+Default workload: the depth-3 chain setting (bonus + 3 drafts = 4 nodes per request),
+256 requests, 32 heads, d_k = d_v = 128, fp32 state, bf16 q/k/v; several layers' input sets
+are resident and rotated so every step streams its state from HBM (each layer's state is
+512 MiB, larger than the 126 MB L2).
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU fp64 replay oracle instead
+(a deliberately slow baseline), on the same workload, metric and unit.
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no data-path
+collective): the step time is the max over ranks and ``value`` counts all ranks' nodes.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft-node verifications/sec (verify+commit) and achieved HBM GB/s vs B300 peak"
+UNIT = "node-verifications/s"
+KERNEL_SOURCES = {
+    "verify": ["verify_tc.cuh", "verify_simt.cuh", "common.cuh", "ptx.cuh"],
+    "commit": ["commit.cuh", "common.cuh"],
+}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic byte / flop model (per launch)
+# ---------------------------------------------------------------------------
+
+def verify_bytes(tb) -> int:
+    """State read once + per (node, head): q, k, v in; beta, g in; o, U out; G out."""
+    per_node_head = 2 * tb.dk * 2 + tb.dv * 2 + 8 + 2 * tb.dv * 4 + 4
+    return tb.B * tb.H * tb.dk * tb.dv * 4 + tb.T * tb.H * per_node_head + tb.T * 4 + (tb.B + 1) * 4
+
+
+def commit_bytes(tb) -> int:
+    """State read + written once per (request, head) with a non-empty path, plus the path's
+    u (fp32), k (bf16) and G."""
+    L = tb.path_len.astype(np.int64)
+    active = int(np.sum(L > 0))
+    return active * tb.H * 2 * tb.dk * tb.dv * 4 + int(L.sum()) * tb.H * (tb.dv * 4 + tb.dk * 2 + 4)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "source": "fallback"}
+
+
+def kernel_src_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        p = os.path.join(ROOT, "gated_deltanet_tree_03_b300", "csrc", name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source (lines: kernel workload bytes_per_launch src_sha)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_src_sha(kernel)
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
+                    and parts[3] == sha:
+                return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (harness only; the path itself has no collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_layers(rank: int, n_layers: int) -> list[int]:
+    """Input-set (layer) indices owned by one rank: disjoint across ranks, so ranks process
+    independent batches."""
+    return [rank * n_layers + i for i in range(n_layers)]
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def workload_name(cfg: int, batch: int) -> str:
+    return {
+        0: "config0: chain of 3, B=1, H=1, d=32",
+        1: f"config1: depth-3 chain (4 nodes incl. bonus), B={batch}, H=32, d_k=d_v=128, fp32 state, bf16 q/k/v",
+        2: f"config2: 6-node root-branch tree, B={batch}, H=48, d=128",
+        3: f"config3: ragged random trees of 16-64 nodes, B={batch}, H=32, d=128",
+        4: f"config4: 32-node random trees, B={batch}, H=32, d=128, gate a~U(0.85,1)",
+    }[cfg]
+
+
+def make_layers(cfg: int, batch: int, layer_ids):
+    from gated_deltanet_tree_03_b300 import workloads as W
+    return [W.make_config(cfg, batch=batch, layer=l) for l in layer_ids]
+
+
+def sub_batch(tb, r0: int, r1: int):
+    """Requests r0..r1-1 of a TreeBatch (all heads), as a new TreeBatch."""
+    from gated_deltanet_tree_03_b300.workloads import TreeBatch
+    t0, t1 = int(tb.cu_nodes[r0]), int(tb.cu_nodes[r1])
+    return TreeBatch(B=r1 - r0, H=tb.H, dk=tb.dk, dv=tb.dv, parent=tb.parent[t0:t1].copy(),
+                     cu_nodes=(tb.cu_nodes[r0:r1 + 1] - t0).astype(np.int32), path=tb.path[r0:r1].copy(),
+                     path_len=tb.path_len[r0:r1].copy(), ST0=tb.ST0[r0:r1].copy(), q=tb.q[t0:t1].copy(),
+                     k=tb.k[t0:t1].copy(), v=tb.v[t0:t1].copy(), beta=tb.beta[t0:t1].copy(),
+                     g=tb.g[t0:t1].copy(), name=tb.name + f"[{r0}:{r1}]")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step(sb):
+    import oracle
+    inp = oracle.batch_inputs(sb)
+    oracle.verify(**inp)
+    oracle.commit(inp["ST0"], inp["k"], inp["v"], inp["beta"], inp["g"], sb.parent, sb.cu_nodes, sb.path,
+                  sb.path_len)
+
+
+def cpu_baseline(tb, target_s: float = 12.0) -> dict:
+    """Time the oracle as it stands (OpenMP over pairs, all host cores) on a bounded sample of
+    the workload: the first R requests with all heads, R sized for about target_s seconds."""
+    import oracle
+    one = sub_batch(tb, 0, 1)
+    t = time.perf_counter()
+    oracle_step(one)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    R = int(max(1, min(tb.B, target_s / t1)))
+    sb = sub_batch(tb, 0, R)
+    t = time.perf_counter()
+    oracle_step(sb)
+    dt = time.perf_counter() - t
+    nodes = int(sb.cu_nodes[-1])
+    return {"value": nodes / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"first {R} of {tb.B} requests x all {tb.H} heads (verify + commit replay, fp64), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    tb = make_layers(args.config, args.batch, [0])[0]
+    steps, warmup = args.steps, args.warmup
+    R = args.ref_requests
+    samples = [sub_batch(tb, (i * R) % tb.B, (i * R) % tb.B + R) for i in range(min(tb.B // R, 64))]
+    for i in range(warmup):
+        oracle_step(samples[i % len(samples)])
+    nodes = 0
+    t = time.perf_counter()
+    for i in range(steps):
+        sb = samples[i % len(samples)]
+        oracle_step(sb)
+        nodes += int(sb.cu_nodes[-1])
+    dt = time.perf_counter() - t
+    value = nodes / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(args.config, tb.B), "sample_per_step": f"{R} request(s) x {tb.H} heads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": f"{R} request(s) x all {tb.H} heads per step, verify + commit replay"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+
+    from gated_deltanet_tree_03_b300 import binding as gb
+    from gated_deltanet_tree_03_b300 import device as gd
+
+    layers = make_layers(args.config, args.batch, shard_layers(rank, args.layers))
+    tb0 = layers[0]
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(tb0)
+
+    verify_fn = {"wy": gb.gdn_tree_verify, "simt": gb.gdn_tree_verify_simt}[args.kernel]
+    dev_in = [gd.upload(tb, device=dev) for tb in layers]
+    dev_out = [gd.alloc_outputs(tb, device=dev) for tb in layers]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        tb, d, o = layers[i % len(layers)], dev_in[i % len(layers)], dev_out[i % len(layers)]
+        verify_fn(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], tb.B, tb.H,
+                  tb.dk, tb.dv, tb.max_nodes, o["o"], o["U"], o["G"], o["status"], stream)
+        return tb, d, o
+
+    def commit(tb, d, o):
+        gb.gdn_tree_commit(d["ST"], o["U"], o["G"], d["k"], d["parent"], d["cu_nodes"], d["path"], d["path_len"],
+                           tb.B, tb.H, tb.dk, tb.dv, tb.max_path, o["status"], stream)
+
+    for i in range(args.warmup):
+        commit(*step(i))
+    torch.cuda.synchronize()
+    status = sum(int(o["status"][0].item()) for o in dev_out)
+    if status:
+        raise RuntimeError(f"device reported data errors (status bits {status:#x})")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        ev[i][0].record(stream)
+        tb, d, o = step(i)
+        ev[i][1].record(stream)
+        commit(tb, d, o)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    t_ver = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    t_com = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    nodes_per_step = tb0.T  # draft nodes of one layer's batch, all heads
+    value = nodes_per_step * world * K / (total_ms / 1e3)
+
+    peaks = measured_peaks()
+    vb = float(np.mean([verify_bytes(tb) for tb in layers]))
+    cb = float(np.mean([commit_bytes(tb) for tb in layers]))
+    v_ms, c_ms = t_ver / K, t_com / K
+    kernels = {
+        "verify": {"ms": v_ms, "alg_bytes": vb, "GB/s": vb / (v_ms * 1e6), "frac": vb / (v_ms * 1e6) / peaks["hbm_gbs"]},
+        "commit": {"ms": c_ms, "alg_bytes": cb, "GB/s": cb / (c_ms * 1e6), "frac": cb / (c_ms * 1e6) / peaks["hbm_gbs"]},
+        "verify+commit": {"ms": v_ms + c_ms, "GB/s": (vb + cb) / ((v_ms + c_ms) * 1e6),
+                          "frac": (vb + cb) / ((v_ms + c_ms) * 1e6) / peaks["hbm_gbs"]},
+    }
+    dom = "verify" if v_ms >= c_ms else "commit"
+    wl = f"config{args.config}"
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["GB/s"], "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_source": peaks["source"],
+                "traffic": ncu_traffic(dom, wl)}
+
+    # end to end: pinned host inputs -> device, verify + commit, outputs -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        keys = ["q", "k", "v", "beta", "g", "parent", "cu_nodes", "path", "path_len"]
+        host_in = [gd.upload(tb, pin=True) for tb in layers]
+        host_o = [torch.empty_like(o["o"], device="cpu").pin_memory() for o in dev_out]
+        h2d = sum(host_in[0][k].numel() * host_in[0][k].element_size() for k in keys)
+        d2h = host_o[0].numel() * host_o[0].element_size()
+        Ke = max(1, min(K, args.e2e_steps))
+
+        def e2e_step(i):
+            j = i % len(layers)
+            for k in keys:
+                dev_in[j][k].copy_(host_in[j][k], non_blocking=True)
+            commit(*step(i))
+            host_o[j].copy_(dev_out[j]["o"], non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(Ke):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(dist, e0.elapsed_time(e1), dev)
+        e2e = {"value": nodes_per_step * world * Ke / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "note": "state resident in HBM across steps; per-step node block, tree and paths copied in, o copied out"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_name(args.config, tb0.B), "batch_per_gpu": tb0.B, "heads": tb0.H,
+                       "d_k": tb0.dk, "d_v": tb0.dv, "nodes_per_layer": nodes_per_step,
+                       "layers_rotated": len(layers), "verify_kernel": args.kernel,
+                       "l2": "inputs larger than L2 (per-layer state > 126 MB; layers rotated)",
+                       "parallelism": f"dp{world} (independent batches per GPU)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clk,
+            "kernels": kernels, "wall_s_timed": wall}
+    if rank == 0:
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--kernel", choices=["wy", "simt"], default="wy")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--ref-requests", type=int, default=1)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

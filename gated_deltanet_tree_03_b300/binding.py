@@ -1,0 +1,140 @@
+"""Thin ctypes binding of libgdn_tree.so (declared in include/gdn_tree.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels behind
+the C ABI. Array arguments may be CUDA ``torch.Tensor`` objects (their device pointer is
+passed), plain integer device addresses, or ``None`` (NULL). ``stream`` defaults to torch's
+current CUDA stream. A non-GDN_OK return code raises ``GdnError``. If the shared library is
+missing and cannot be built, importing this module raises - there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import re
+import os
+
+from . import _build
+
+GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
+STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT = 1, 2, 4, 8
+MAX_NODES = 64
+
+HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, fn: str):
+        self.code = int(code)
+        super().__init__(f"{fn}: {status_str(code)}")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+_lib = _load()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+
+_SIGS = {
+    "gdn_tree_verify": [_P] * 8 + [_I] * 5 + [_P] * 4 + [_P],
+    "gdn_tree_verify_simt": [_P] * 8 + [_I] * 5 + [_P] * 4 + [_P],
+    "gdn_tree_commit": [_P] * 8 + [_I] * 5 + [_P, _P],
+    "gdn_tree_verify_storeall": [_P] * 8 + [_I] * 5 + [_P] * 5 + [_P],
+    "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 5 + [_P, _P],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.gdn_status_str.argtypes = [ctypes.c_int]
+_lib.gdn_status_str.restype = ctypes.c_char_p
+_lib.gdn_abi_version.argtypes = []
+_lib.gdn_abi_version.restype = ctypes.c_int32
+
+
+def declared_symbols() -> list[str]:
+    """Names of every function the public header declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_0-9]+)\s*\(", text)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_cuda:
+            raise ValueError("array arguments must be CUDA tensors (device memory)")
+        if not x.is_contiguous():
+            raise ValueError("array arguments must be contiguous")
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x)} as a device pointer")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def status_str(code: int) -> str:
+    return _lib.gdn_status_str(int(code)).decode()
+
+
+def abi_version() -> int:
+    return int(_lib.gdn_abi_version())
+
+
+def _check(rc: int, fn: str) -> None:
+    if rc != GDN_OK:
+        raise GdnError(rc, fn)
+
+
+def gdn_tree_verify(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, o, U, G,
+                    status=None, stream=None):
+    _check(_lib.gdn_tree_verify(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent),
+                                _ptr(cu_nodes), B, H, d_k, d_v, max_nodes, _ptr(o), _ptr(U), _ptr(G),
+                                _ptr(status), _stream(stream)), "gdn_tree_verify")
+
+
+def gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, o, U, G,
+                         status=None, stream=None):
+    _check(_lib.gdn_tree_verify_simt(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                     _ptr(parent), _ptr(cu_nodes), B, H, d_k, d_v, max_nodes, _ptr(o),
+                                     _ptr(U), _ptr(G), _ptr(status), _stream(stream)),
+           "gdn_tree_verify_simt")
+
+
+def gdn_tree_commit(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path,
+                    status=None, stream=None):
+    _check(_lib.gdn_tree_commit(_ptr(ST), _ptr(U), _ptr(G), _ptr(k), _ptr(parent), _ptr(cu_nodes),
+                                _ptr(path), _ptr(path_len), B, H, d_k, d_v, max_path, _ptr(status),
+                                _stream(stream)), "gdn_tree_commit")
+
+
+def gdn_tree_verify_storeall(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes,
+                             snapshots, o, U, G, status=None, stream=None):
+    _check(_lib.gdn_tree_verify_storeall(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                         _ptr(parent), _ptr(cu_nodes), B, H, d_k, d_v, max_nodes,
+                                         _ptr(snapshots), _ptr(o), _ptr(U), _ptr(G), _ptr(status),
+                                         _stream(stream)), "gdn_tree_verify_storeall")
+
+
+def gdn_tree_commit_storeall(ST, snapshots, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path,
+                             status=None, stream=None):
+    _check(_lib.gdn_tree_commit_storeall(_ptr(ST), _ptr(snapshots), _ptr(parent), _ptr(cu_nodes),
+                                         _ptr(path), _ptr(path_len), B, H, d_k, d_v, max_path,
+                                         _ptr(status), _stream(stream)), "gdn_tree_commit_storeall")

@@ -1,0 +1,161 @@
+/*
+ * gdn_tree.h - C ABI of the B300 (sm_103a) draft-tree verification library for
+ * Gated DeltaNet (GDN) layers.
+ *
+ * The operation (TreeWY: Speculative Verification for Gated DeltaNet Hybrids, method and
+ * novelty sections; GDN Tree-Scan abstract): given one committed recurrent state per
+ * (request, head) and a parent-before-child draft tree per request, produce every draft
+ * node's output as if the gated delta rule
+ *
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,     o_t = S_t q_t,
+ *
+ * had been replayed along that node's root-to-node path (a_t = exp(g_t)), without storing a
+ * state per node; then, once a path is accepted, rebuild only that path's state.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array arguments are DEVICE pointers owned by the caller. The library allocates
+ *    nothing, keeps no state between calls and never synchronises the device: each call
+ *    validates its scalar arguments on the host, enqueues its kernels on `stream` and
+ *    returns. Results are valid once the stream has reached that point.
+ *  - Layouts (T = total draft nodes = cu_nodes[B], all row-major, innermost last):
+ *        ST        [B][H][d_k][d_v]  fp32   committed state S^T (S is d_v x d_k)
+ *        q, k      [T][H][d_k]       bf16   (passed as uint16_t bit patterns)
+ *        v         [T][H][d_v]       bf16
+ *        beta, g   [T][H]            fp32   g = ln a (natural log of the gate, <= 0)
+ *        parent    [T]               int32  request-local parent index, -1 = child of the
+ *                                           committed state; parent[t] < t (topological order)
+ *        cu_nodes  [B+1]             int32  node offsets; request r owns nodes
+ *                                           cu_nodes[r] .. cu_nodes[r+1]-1 (0..64 nodes)
+ *        o, U      [T][H][d_v]       fp32   outputs / pseudo-values
+ *        G         [T][H]            fp32   cumulative log-gate over the root-to-node path
+ *        path      [B][max_path]     int32  accepted path, request-local ids, root first
+ *        path_len  [B]               int32  0 = keep the committed state unchanged
+ *    One tree is shared by all heads of a request; each head has its own q/k/v/beta/g.
+ *  - Sizes: d_k, d_v in {32, 64, 128}; 0 <= nodes per request <= max_nodes <= 64;
+ *    max_path <= 64. B may be 0 (nothing is launched).
+ *  - Alignment: every array must be 16-byte aligned.
+ *  - Errors: argument errors are reported by the return value before anything is launched.
+ *    Data errors that only the device can see (a parent index outside [-1, t-1], a request
+ *    with more than max_nodes nodes, an accepted path that is not a root-to-node chain) are
+ *    OR-ed into `*status` as GDN_STATUS_* bits when `status` is non-NULL; the affected
+ *    request writes nothing (no outputs, state left as it was). Kernels never trap.
+ *  - Concurrency: verify only reads ST, so verifies may share a state. A commit writes ST in
+ *    place and must not overlap a verify or commit of the same request on another stream.
+ */
+#ifndef GDN_TREE_H
+#define GDN_TREE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_EINVAL = 1,      /* null pointer, negative size, unsupported d_k / d_v              */
+    GDN_ETOOBIG = 2,     /* max_nodes > 64 or max_path > 64                                  */
+    GDN_EALIGN = 3,      /* an array is not 16-byte aligned                                  */
+    GDN_ECUDA = 6,       /* a CUDA runtime call failed (no device, launch failure, ...)      */
+    GDN_EARCH = 7        /* the current device cannot run sm_103a code                       */
+} gdn_status;
+
+/* Device-side data error bits, OR-ed into *status. */
+#define GDN_STATUS_BAD_TREE 1u       /* parent[t] outside [-1, t-1]                          */
+#define GDN_STATUS_BAD_PATH 2u       /* accepted path is not a root-to-node chain            */
+#define GDN_STATUS_TOO_MANY_NODES 4u /* a request has more than max_nodes nodes              */
+#define GDN_STATUS_TIMEOUT 8u        /* a bounded wait on an asynchronous copy gave up       */
+
+/*
+ * gdn_tree_verify - outputs and pseudo-values of every draft node (tree-structured WY form).
+ *
+ * Defined by the TreeWY page (method section): pseudo-values of all candidates come from one
+ * triangular system over the parent-before-child ordered tree, a node refers only to its
+ * ancestors, and node outputs follow from the pseudo-values. Written out per (request, head):
+ *     G_t = sum of g over t's root-to-node path,  gamma_t = exp(G_t)
+ *     (I + A) U = R,   A[t,j] = b_t exp(G_t - G_j) (k_t . k_j)   for j a strict ancestor of t
+ *                      R_t    = b_t (v_t - gamma_t S_0 k_t)
+ *     o_t = gamma_t S_0 q_t + sum_{j ancestor of t or t itself} exp(G_t - G_j) (q_t . k_j) u_j
+ * which equals the root-to-node replay of the rule (GDN Tree-Scan abstract) in exact
+ * arithmetic; u_t = b_t (v_t - a_t S_parent(t) k_t) is the node's pseudo-value.
+ *
+ *   ST                 in   committed states, read only
+ *   q, k, v, beta, g   in   node block
+ *   parent, cu_nodes   in   tree shape
+ *   B, H, d_k, d_v     in   sizes; max_nodes = an upper bound on nodes per request
+ *   o, U, G            out  written for every node of every valid request
+ *   status             out  optional device int32, GDN_STATUS_* bits OR-ed in
+ */
+gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k,
+                           const uint16_t *v, const float *beta, const float *g,
+                           const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H,
+                           int32_t d_k, int32_t d_v, int32_t max_nodes, float *o, float *U,
+                           float *G, int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_verify_simt - the same operation and contract as gdn_tree_verify, computed by a
+ * CUDA-core (fp32 FMA) kernel instead of the tensor-core kernel. It exists as an in-run
+ * cross-check of the tensor-core path; results agree within fp32 rounding.
+ */
+gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16_t *k,
+                                const uint16_t *v, const float *beta, const float *g,
+                                const int32_t *parent, const int32_t *cu_nodes, int32_t B,
+                                int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes, float *o,
+                                float *U, float *G, int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_commit - rebuild the accepted path's state in place (TreeWY page, method section:
+ * only the accepted path's pseudo-values are combined into the next committed state; novelty
+ * section: exactly one full state is rebuilt). With l the last node of the path:
+ *     ST <- exp(G_l) ST + sum_{j on the path} exp(G_l - G_j) k_j u_j^T
+ * U and G are the outputs of gdn_tree_verify for the same inputs; k is its key block.
+ * parent and cu_nodes are used to check that path is a root-to-node chain.
+ * path_len[r] == 0 leaves request r's state untouched. Each state element is read once and
+ * written once.
+ */
+gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint16_t *k,
+                           const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
+                           const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
+                           int32_t d_v, int32_t max_path, int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_verify_storeall - the comparison baseline the TreeWY page calls "storeall"
+ * (comparison with prior methods): step every node from its parent's stored state in
+ * topological order and store the state at every node.
+ *     snapshots [T][H][d_k][d_v] fp32 (out): S_t^T for every node t.
+ * o, U and G are produced as by gdn_tree_verify. Needs T * H * d_k * d_v * 4 bytes of
+ * snapshot memory, which is what the WY form avoids.
+ */
+gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,
+                                    const uint16_t *v, const float *beta, const float *g,
+                                    const int32_t *parent, const int32_t *cu_nodes, int32_t B,
+                                    int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes,
+                                    float *snapshots, float *o, float *U, float *G,
+                                    int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_commit_storeall - storeall commit: copy the stored state of the accepted path's
+ * last node into ST (same path checks and path_len == 0 behaviour as gdn_tree_commit).
+ */
+gdn_status gdn_tree_commit_storeall(float *ST, const float *snapshots, const int32_t *parent,
+                                    const int32_t *cu_nodes, const int32_t *path,
+                                    const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
+                                    int32_t d_v, int32_t max_path, int32_t *status,
+                                    gdn_stream_t stream);
+
+/* Human-readable name of a return code (static string, never NULL). */
+const char *gdn_status_str(gdn_status s);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int32_t gdn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_TREE_H */

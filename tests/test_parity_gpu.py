@@ -1,0 +1,200 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 replay oracle.
+
+Covers all five synthetic configurations at their full sizes (sampled (request, head) pairs
+for the oracle where the whole batch would take it too long), tiny and ragged random trees in
+random topological orders, empty requests, the deepest (chain of 64) and widest (star of 64)
+trees, forests, both verify kernels (tensor-core WY and CUDA-core WY), the store-all
+comparison kernels, and the device-side error reporting.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_tree_03_b300 import binding as gb
+from gated_deltanet_tree_03_b300 import device as gd
+from gated_deltanet_tree_03_b300 import workloads as W
+from gpu_util import check_commit, check_verify, run_gpu, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["wy", "simt"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS + ["storeall"])
+def test_config0_full(kernel):
+    tb = W.make_config(0)
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    check_verify(tb, res, tag=f"config0/{kernel}")
+    check_commit(tb, res, tag=f"config0/{kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config1_full_size_sampled(kernel):
+    tb = W.make_config(1)  # B=256, H=32, d=128, chain of 4
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["U"]))
+    pairs = sample_pairs(tb, 96, seed=1)
+    check_verify(tb, res, pairs, tag=f"config1/{kernel}")
+    check_commit(tb, res, pairs, tag=f"config1/{kernel}")
+
+
+@pytest.mark.parametrize("batch", [1, 64])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config2(batch, kernel):
+    tb = W.make_config(2, batch=batch)
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    pairs = None if batch == 1 else sample_pairs(tb, 96, seed=2)
+    check_verify(tb, res, pairs, tag=f"config2/B{batch}/{kernel}")
+    check_commit(tb, res, pairs, tag=f"config2/B{batch}/{kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_config3_ragged_full_size_sampled(kernel):
+    tb = W.make_config(3)
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    assert np.all(np.isfinite(res["o"]))
+    pairs = sample_pairs(tb, 64, seed=3)
+    check_verify(tb, res, pairs, tag=f"config3/{kernel}")
+    check_commit(tb, res, pairs, tag=f"config3/{kernel}")
+
+
+@pytest.mark.parametrize("batch", [1, 8, 512])
+def test_config4(batch):
+    tb = W.make_config(4, batch=batch, layer=batch % 48)
+    res = run_gpu(tb, verify="wy")
+    assert res["status"] == 0
+    pairs = sample_pairs(tb, 64, seed=4)
+    check_verify(tb, res, pairs, tag=f"config4/B{batch}")
+    check_commit(tb, res, pairs, tag=f"config4/B{batch}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("kernel", KERNELS + ["storeall"])
+def test_random_ragged_trees(d, kernel):
+    tb = W.make_random_batch(seed=100 + d, B=9, H=3, d=d, n_range=(1, 64), fanout_max=4, depth_max=8,
+                             empty_every=4)
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    check_verify(tb, res, tag=f"random/d{d}/{kernel}")
+    check_commit(tb, res, tag=f"random/d{d}/{kernel}")
+
+
+@pytest.mark.parametrize("shape", ["chain64", "star64", "forest"])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_extreme_shapes(shape, kernel):
+    rng = np.random.default_rng(7)
+    if shape == "chain64":
+        parents = [W.chain_parents(64), W.chain_parents(33)]
+        paths = [list(range(64)), list(range(20))]
+    elif shape == "star64":
+        parents = [np.array([-1] + [0] * 63, np.int32)]
+        paths = [[0, 17]]
+    else:  # several roots per request, random topological order
+        p = np.array([-1, -1, 0, 1, 2, -1, 3, 5, 5, 6], np.int32)
+        p, _ = W.random_topological_relabel(rng, p)
+        parents = [p]
+        leaf = W.leaves(p)[0]
+        paths = [W.root_path(p, leaf)]
+    tb = W.build_batch(rng, parents, paths, H=2, dk=128, dv=128)
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] == 0
+    check_verify(tb, res, tag=f"{shape}/{kernel}")
+    check_commit(tb, res, tag=f"{shape}/{kernel}")
+
+
+def test_kernels_agree_and_snapshots_are_states():
+    """Tensor-core WY, CUDA-core WY and store-all agree; store-all snapshots are replay states."""
+    import oracle
+    tb = W.make_random_batch(seed=5, B=4, H=2, d=64, n_range=(4, 20))
+    a = run_gpu(tb, verify="wy", commit=False)
+    b = run_gpu(tb, verify="simt", commit=False)
+    c = run_gpu(tb, verify="storeall", commit=False)
+    scale = np.max(np.abs(c["o"])) + 1
+    assert np.max(np.abs(a["o"] - b["o"])) <= 2e-3 * scale
+    assert np.max(np.abs(a["o"] - c["o"])) <= 2e-3 * scale
+    inp = oracle.batch_inputs(tb)
+    for r in range(tb.B):
+        par = tb.request_parent(r)
+        for t in range(len(par)):
+            pth = W.root_path(par, t)
+            path = np.full((tb.B, 64), -1, np.int32)
+            plen = np.zeros(tb.B, np.int32)
+            path[r, :len(pth)] = pth
+            plen[r] = len(pth)
+            ref = oracle.commit(inp["ST0"], inp["k"], inp["v"], inp["beta"], inp["g"], tb.parent, tb.cu_nodes,
+                                path, plen, pairs=[r * tb.H + h for h in range(tb.H)])
+            got = c["snap"][tb.cu_nodes[r] + t]
+            rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+            assert rel <= 1e-4
+
+
+@pytest.mark.parametrize("kernel", KERNELS + ["storeall"])
+def test_bad_tree_reports_and_skips_only_that_request(kernel):
+    tb = W.make_random_batch(seed=9, B=3, H=2, d=32, n_range=(5, 9))
+    tb.parent[tb.cu_nodes[1] + 3] = 3  # node 3 of request 1 names itself as parent
+    tb.path_len[:] = 0
+    res = run_gpu(tb, verify=kernel, commit=False)
+    assert res["status"] & gb.STATUS_BAD_TREE
+    r1 = slice(tb.cu_nodes[1], tb.cu_nodes[2])
+    assert np.all(np.isnan(res["o"][r1])) and np.all(np.isnan(res["U"][r1]))
+    for r in (0, 2):
+        rs = slice(tb.cu_nodes[r], tb.cu_nodes[r + 1])
+        assert np.all(np.isfinite(res["o"][rs]))
+
+
+@pytest.mark.parametrize("kernel", ["wy", "storeall"])
+def test_bad_path_reports_and_keeps_state(kernel):
+    tb = W.make_config(2, batch=4, heads=2)
+    tb.path[1, :2] = [0, 4]  # 4 is a grandchild of 0, not a child
+    tb.path_len[1] = 2
+    tb.path[2, :1] = [3]  # does not start at the root
+    tb.path_len[2] = 1
+    res = run_gpu(tb, verify=kernel)
+    assert res["status"] & gb.STATUS_BAD_PATH
+    np.testing.assert_array_equal(res["ST"][1], tb.ST0[1])
+    np.testing.assert_array_equal(res["ST"][2], tb.ST0[2])
+    for r in (0, 3):
+        if tb.path_len[r]:
+            assert not np.array_equal(res["ST"][r], tb.ST0[r])
+
+
+def test_too_many_nodes_and_empty_path():
+    tb = W.make_random_batch(seed=10, B=3, H=2, d=64, n_range=(10, 12))
+    tb.path_len[:] = 0
+    res = run_gpu(tb, verify="wy", max_nodes=9)  # every request has more than 9 nodes
+    assert res["status"] & gb.STATUS_TOO_MANY_NODES
+    assert np.all(np.isnan(res["o"]))
+    np.testing.assert_array_equal(res["ST"], tb.ST0)  # path_len == 0 keeps the state bit for bit
+
+
+def test_host_argument_errors():
+    tb = W.make_config(0)
+    d = gd.upload(tb)
+    out = gd.alloc_outputs(tb)
+    base = [d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], 1, 1, 32, 32, 3,
+            out["o"], out["U"], out["G"]]
+    bad = list(base)
+    bad[12] = 65
+    with pytest.raises(gb.GdnError) as e:
+        gb.gdn_tree_verify(*bad)
+    assert e.value.code == gb.GDN_ETOOBIG
+    bad = list(base)
+    bad[10] = 48
+    with pytest.raises(gb.GdnError) as e:
+        gb.gdn_tree_verify(*bad)
+    assert e.value.code == gb.GDN_EINVAL
+    bad = list(base)
+    bad[0] = d["ST"].data_ptr() + 4
+    with pytest.raises(gb.GdnError) as e:
+        gb.gdn_tree_verify(*bad)
+    assert e.value.code == gb.GDN_EALIGN
+    # B == 0 launches nothing and succeeds
+    empty = list(base)
+    empty[8] = 0
+    gb.gdn_tree_verify(*empty)
+    torch.cuda.synchronize()
