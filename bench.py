@@ -297,12 +297,12 @@ def run_ours(args):
     def step(i):
         tb, d, o = layers[i % len(layers)], dev_in[i % len(layers)], dev_out[i % len(layers)]
         verify_fn(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], tb.B, tb.H,
-                  tb.dk, tb.dv, tb.max_nodes, o["o"], o["U"], o["G"], o["status"], stream)
+                  tb.T, tb.dk, tb.dv, tb.max_nodes, o["o"], o["U"], o["G"], o["status"], stream)
         return tb, d, o
 
     def commit(tb, d, o):
         gb.gdn_tree_commit(d["ST"], o["U"], o["G"], d["k"], d["parent"], d["cu_nodes"], d["path"], d["path_len"],
-                           tb.B, tb.H, tb.dk, tb.dv, tb.max_path, o["status"], stream)
+                           tb.B, tb.H, tb.T, tb.dk, tb.dv, tb.max_path, o["status"], stream)
 
     for i in range(args.warmup):
         commit(*step(i))

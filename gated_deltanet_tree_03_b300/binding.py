@@ -16,7 +16,7 @@ import os
 from . import _build
 
 GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
-STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT = 1, 2, 4, 8
+STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8, 16
 MAX_NODES = 64
 
 HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
@@ -39,11 +39,11 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int32
 
 _SIGS = {
-    "gdn_tree_verify": [_P] * 8 + [_I] * 5 + [_P] * 4 + [_P],
-    "gdn_tree_verify_simt": [_P] * 8 + [_I] * 5 + [_P] * 4 + [_P],
-    "gdn_tree_commit": [_P] * 8 + [_I] * 5 + [_P, _P],
-    "gdn_tree_verify_storeall": [_P] * 8 + [_I] * 5 + [_P] * 5 + [_P],
-    "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 5 + [_P, _P],
+    "gdn_tree_verify": [_P] * 8 + [_I] * 6 + [_P] * 4 + [_P],
+    "gdn_tree_verify_simt": [_P] * 8 + [_I] * 6 + [_P] * 4 + [_P],
+    "gdn_tree_commit": [_P] * 8 + [_I] * 6 + [_P, _P],
+    "gdn_tree_verify_storeall": [_P] * 8 + [_I] * 6 + [_P] * 5 + [_P],
+    "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 6 + [_P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -103,38 +103,38 @@ def _check(rc: int, fn: str) -> None:
         raise GdnError(rc, fn)
 
 
-def gdn_tree_verify(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, o, U, G,
+def gdn_tree_verify(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G,
                     status=None, stream=None):
     _check(_lib.gdn_tree_verify(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent),
-                                _ptr(cu_nodes), B, H, d_k, d_v, max_nodes, _ptr(o), _ptr(U), _ptr(G),
+                                _ptr(cu_nodes), B, H, T, d_k, d_v, max_nodes, _ptr(o), _ptr(U), _ptr(G),
                                 _ptr(status), _stream(stream)), "gdn_tree_verify")
 
 
-def gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, o, U, G,
+def gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G,
                          status=None, stream=None):
     _check(_lib.gdn_tree_verify_simt(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                     _ptr(parent), _ptr(cu_nodes), B, H, d_k, d_v, max_nodes, _ptr(o),
+                                     _ptr(parent), _ptr(cu_nodes), B, H, T, d_k, d_v, max_nodes, _ptr(o),
                                      _ptr(U), _ptr(G), _ptr(status), _stream(stream)),
            "gdn_tree_verify_simt")
 
 
-def gdn_tree_commit(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path,
+def gdn_tree_commit(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path,
                     status=None, stream=None):
     _check(_lib.gdn_tree_commit(_ptr(ST), _ptr(U), _ptr(G), _ptr(k), _ptr(parent), _ptr(cu_nodes),
-                                _ptr(path), _ptr(path_len), B, H, d_k, d_v, max_path, _ptr(status),
+                                _ptr(path), _ptr(path_len), B, H, T, d_k, d_v, max_path, _ptr(status),
                                 _stream(stream)), "gdn_tree_commit")
 
 
-def gdn_tree_verify_storeall(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes,
+def gdn_tree_verify_storeall(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes,
                              snapshots, o, U, G, status=None, stream=None):
     _check(_lib.gdn_tree_verify_storeall(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
-                                         _ptr(parent), _ptr(cu_nodes), B, H, d_k, d_v, max_nodes,
+                                         _ptr(parent), _ptr(cu_nodes), B, H, T, d_k, d_v, max_nodes,
                                          _ptr(snapshots), _ptr(o), _ptr(U), _ptr(G), _ptr(status),
                                          _stream(stream)), "gdn_tree_verify_storeall")
 
 
-def gdn_tree_commit_storeall(ST, snapshots, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path,
+def gdn_tree_commit_storeall(ST, snapshots, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path,
                              status=None, stream=None):
     _check(_lib.gdn_tree_commit_storeall(_ptr(ST), _ptr(snapshots), _ptr(parent), _ptr(cu_nodes),
-                                         _ptr(path), _ptr(path_len), B, H, d_k, d_v, max_path,
+                                         _ptr(path), _ptr(path_len), B, H, T, d_k, d_v, max_path,
                                          _ptr(status), _stream(stream)), "gdn_tree_commit_storeall")

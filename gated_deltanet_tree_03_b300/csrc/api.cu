@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/gdn_tree.h: argument checks, launch
-// configuration and kernel dispatch. Nothing here allocates, synchronises or keeps state.
+// configuration, TMA descriptor encoding and kernel dispatch. Nothing here allocates device
+// memory, synchronises the device or keeps per-call state.
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "gdn_tree.h"
@@ -10,6 +13,7 @@
 #include "commit.cuh"
 #include "storeall.cuh"
 #include "verify_simt.cuh"
+#include "verify_tc.cuh"
 
 using namespace gdn;
 
@@ -42,13 +46,13 @@ gdn_status launch_status() {
 gdn_status check_verify_args(const float *ST, const uint16_t *q, const uint16_t *k,
                              const uint16_t *v, const float *beta, const float *g,
                              const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H,
-                             int32_t d_k, int32_t d_v, int32_t max_nodes, const float *o,
+                             int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes, const float *o,
                              const float *U, const float *G, const int32_t *status) {
-  if (B < 0 || H <= 0 || max_nodes < 0) return GDN_EINVAL;
-  if (B > 65535 || H > 65535) return GDN_EINVAL;  // grid y / z limits
+  if (B < 0 || H <= 0 || T < 0 || max_nodes < 0) return GDN_EINVAL;
+  if (B > 65535 || H > 65535) return GDN_EINVAL;  // grid limits
   if (!valid_d(d_k) || !valid_d(d_v)) return GDN_EINVAL;
   if (max_nodes > kMaxNodes) return GDN_ETOOBIG;
-  if (B == 0) return GDN_OK;
+  if (B == 0 || T == 0) return GDN_OK;
   if (!ST || !q || !k || !v || !beta || !g || !parent || !cu_nodes || !o || !U || !G)
     return GDN_EINVAL;
   const void *ptrs[] = {ST, q, k, v, beta, g, parent, cu_nodes, o, U, G};
@@ -60,31 +64,79 @@ gdn_status check_verify_args(const float *ST, const uint16_t *q, const uint16_t 
 
 gdn_status check_commit_args(const float *ST, const void *a1, const void *a2, const void *a3,
                              const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
-                             const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
+                             const int32_t *path_len, int32_t B, int32_t H, int32_t T, int32_t d_k,
                              int32_t d_v, int32_t max_path, const int32_t *status) {
-  if (B < 0 || H <= 0 || max_path < 0) return GDN_EINVAL;
+  if (B < 0 || H <= 0 || T < 0 || max_path < 0) return GDN_EINVAL;
   if (!valid_d(d_k) || !valid_d(d_v)) return GDN_EINVAL;
   if (max_path > kMaxNodes) return GDN_ETOOBIG;
   if (B == 0) return GDN_OK;
-  if (!ST || !a1 || !a2 || !a3 || !parent || !cu_nodes || !path_len) return GDN_EINVAL;
+  if (!ST || !cu_nodes || !path_len) return GDN_EINVAL;
+  if (T > 0 && (!a1 || !a2 || !a3 || !parent)) return GDN_EINVAL;
   if (max_path > 0 && !path) return GDN_EINVAL;
-  const void *ptrs[] = {ST, a1, a2, a3, parent, cu_nodes, path_len};
+  const void *ptrs[] = {ST, a1, a2, a3, parent, cu_nodes, path_len, path, status};
   for (const void *p : ptrs)
-    if (!aligned16(p)) return GDN_EALIGN;
-  if (path && !aligned16(path)) return GDN_EALIGN;
-  if (status && !aligned16(status)) return GDN_EALIGN;
+    if (p && !aligned16(p)) return GDN_EALIGN;
   return GDN_OK;
+}
+
+// ------------------------------------------------------------------ TMA descriptors
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [T][H][D] bf16 rows viewed as a 3-D tensor (D, H, T); box = (box0, 1, rows)
+bool encode_rows(CUtensorMap *map, const uint16_t *base, int D, int H, int T, int box0, int rows,
+                 CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(T)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(H) * D * 2};
+  const cuuint32_t box[3] = {cuuint32_t(box0), 1u, cuuint32_t(rows)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int DK>
 gdn_status launch_verify_simt(const VerifyArgs &a, cudaStream_t stream) {
-  const int M = a.max_nodes;
-  const size_t smem = verify_simt_smem_bytes(M, DK);
+  const size_t smem = verify_simt_smem_bytes(a.max_nodes, DK);
   if (cudaFuncSetAttribute(verify_simt_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return GDN_ECUDA;
   dim3 grid(a.dv / 32, a.H, a.B);
   verify_simt_kernel<DK><<<grid, kThreads, smem, stream>>>(a);
+  return launch_status();
+}
+
+template <int DK, int DV>
+gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
+  const int Np = ((a.max_nodes < 1 ? 1 : a.max_nodes) + 15) / 16 * 16;
+  CUtensorMap tk, tq, tv;
+  if (!encode_rows(&tk, a.k, DK, a.H, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tq, a.q, DK, a.H, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tv, a.v, DV, a.H, a.T, DV, Np, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return GDN_ECUDA;
+  const size_t smem = tc_smem_bytes(DK, DV, Np);
+  if (cudaFuncSetAttribute(verify_tc_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem)) != cudaSuccess)
+    return GDN_ECUDA;
+  const long long blocks = (long long)a.B * a.H;
+  verify_tc_kernel<DK, DV><<<unsigned(blocks), kThreads, smem, stream>>>(tk, tq, tv, a, Np);
   return launch_status();
 }
 
@@ -99,7 +151,7 @@ gdn_status launch_storeall(const StoreallArgs &a, cudaStream_t stream) {
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return 1; }
+int32_t gdn_abi_version(void) { return 2; }
 
 const char *gdn_status_str(gdn_status s) {
   switch (s) {
@@ -116,13 +168,14 @@ const char *gdn_status_str(gdn_status s) {
 gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16_t *k,
                                 const uint16_t *v, const float *beta, const float *g,
                                 const int32_t *parent, const int32_t *cu_nodes, int32_t B,
-                                int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes, float *o,
-                                float *U, float *G, int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v,
+                                int32_t H, int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes,
+                                float *o, float *U, float *G, int32_t *status,
+                                gdn_stream_t stream) {
+  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
                                     max_nodes, o, U, G, status);
-  if (st != GDN_OK || B == 0) return st;
+  if (st != GDN_OK || B == 0 || T == 0) return st;
   if ((st = check_device()) != GDN_OK) return st;
-  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, o, U, G, status};
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (d_k) {
     case 32: return launch_verify_simt<32>(a, s);
@@ -133,22 +186,32 @@ gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16
 
 gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                            const float *beta, const float *g, const int32_t *parent,
-                           const int32_t *cu_nodes, int32_t B, int32_t H, int32_t d_k,
+                           const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T, int32_t d_k,
                            int32_t d_v, int32_t max_nodes, float *o, float *U, float *G,
                            int32_t *status, gdn_stream_t stream) {
-  return gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes,
-                              o, U, G, status, stream);
+  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
+                                    max_nodes, o, U, G, status);
+  if (st != GDN_OK || B == 0 || T == 0) return st;
+  if (d_k == 32 || d_v == 32)
+    return gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o,
+                                U, G, status, stream);
+  if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d_k == 128) return d_v == 128 ? launch_verify_tc<128, 128>(a, s) : launch_verify_tc<128, 64>(a, s);
+  return d_v == 128 ? launch_verify_tc<64, 128>(a, s) : launch_verify_tc<64, 64>(a, s);
 }
 
 gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint16_t *k,
                            const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
-                           const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
+                           const int32_t *path_len, int32_t B, int32_t H, int32_t T, int32_t d_k,
                            int32_t d_v, int32_t max_path, int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_commit_args(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, d_k, d_v,
+  gdn_status st = check_commit_args(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v,
                                     max_path, status);
   if (st != GDN_OK || B == 0) return st;
   if ((st = check_device()) != GDN_OK) return st;
-  CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path, status};
+  CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
   const size_t smem = commit_smem_bytes(max_path, d_k, d_v);
   if (cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
@@ -163,16 +226,17 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,
                                     const uint16_t *v, const float *beta, const float *g,
                                     const int32_t *parent, const int32_t *cu_nodes, int32_t B,
-                                    int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes,
-                                    float *snapshots, float *o, float *U, float *G,
-                                    int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v,
+                                    int32_t H, int32_t T, int32_t d_k, int32_t d_v,
+                                    int32_t max_nodes, float *snapshots, float *o, float *U,
+                                    float *G, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
                                     max_nodes, o, U, G, status);
-  if (st != GDN_OK || B == 0) return st;
+  if (st != GDN_OK || B == 0 || T == 0) return st;
   if (!snapshots) return GDN_EINVAL;
   if (!aligned16(snapshots)) return GDN_EALIGN;
   if ((st = check_device()) != GDN_OK) return st;
-  StoreallArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, d_k, d_v, max_nodes, snapshots, o, U, G, status};
+  StoreallArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, snapshots, o, U, G,
+                 status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (d_k) {
     case 32: return launch_storeall<32>(a, s);
@@ -183,14 +247,14 @@ gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const ui
 
 gdn_status gdn_tree_commit_storeall(float *ST, const float *snapshots, const int32_t *parent,
                                     const int32_t *cu_nodes, const int32_t *path,
-                                    const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
-                                    int32_t d_v, int32_t max_path, int32_t *status,
+                                    const int32_t *path_len, int32_t B, int32_t H, int32_t T,
+                                    int32_t d_k, int32_t d_v, int32_t max_path, int32_t *status,
                                     gdn_stream_t stream) {
   gdn_status st = check_commit_args(ST, snapshots, snapshots, snapshots, parent, cu_nodes, path,
-                                    path_len, B, H, d_k, d_v, max_path, status);
+                                    path_len, B, H, T, d_k, d_v, max_path, status);
   if (st != GDN_OK || B == 0) return st;
   if ((st = check_device()) != GDN_OK) return st;
-  StoreallCommitArgs a{ST, snapshots, parent, cu_nodes, path, path_len, B, H, d_k, d_v, max_path, status};
+  StoreallCommitArgs a{ST, snapshots, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
   const int per_cta = kThreads * 4;
   const long long nchunk = (d_k * d_v / 4 + per_cta - 1) / per_cta;
   const long long blocks = (long long)B * H * nchunk;

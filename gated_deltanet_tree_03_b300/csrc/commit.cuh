@@ -17,7 +17,7 @@ struct CommitArgs {
   const float *U, *G;
   const uint16_t *k;
   const int32_t *parent, *cu_nodes, *path, *path_len;
-  int B, H, dk, dv, max_path;
+  int B, H, T, dk, dv, max_path;
   int32_t *status;
 };
 
@@ -44,6 +44,10 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
   if (L == 0) return;  // keep the committed state
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
+  if (!offsets_ok(t0, n, a.T)) {
+    if (tid == 0 && blockIdx.x % (nchunk * a.H) == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+    return;
+  }
   const int dv4 = a.dv >> 2;
   const int nf = KR * dv4;
   float4 *slab = reinterpret_cast<float4 *>(a.ST + ((size_t(r) * a.H + h) * a.dk + size_t(chunk) * KR) * a.dv);

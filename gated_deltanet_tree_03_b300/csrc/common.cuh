@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "gdn_tree.h"
@@ -16,6 +17,9 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_floa
 __device__ __forceinline__ void report(int32_t *status, unsigned bit) {
   if (status != nullptr) atomicOr(reinterpret_cast<int *>(status), int(bit));
 }
+
+// Request r's node range [t0, t0 + n) must lie inside the T allocated node rows.
+__device__ __forceinline__ bool offsets_ok(int t0, int n, int T) { return t0 >= 0 && n >= 0 && t0 + n <= T; }
 
 // Per-request tree analysis kept in shared memory.
 //   anc[t]  : bit j set <=> j is on t's root-to-node path (t itself included)

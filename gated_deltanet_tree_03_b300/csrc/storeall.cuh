@@ -18,7 +18,7 @@ struct StoreallArgs {
   const uint16_t *q, *k, *v;
   const float *beta, *g;
   const int32_t *parent, *cu_nodes;
-  int B, H, dk, dv, max_nodes;
+  int B, H, T, dk, dv, max_nodes;
   float *snap, *o, *U, *G;
   int32_t *status;
 };
@@ -33,8 +33,12 @@ __global__ void __launch_bounds__(kThreads) verify_storeall_kernel(StoreallArgs 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
+  if (!offsets_ok(t0, n, a.T)) {
+    if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+    return;
+  }
   if (n == 0) return;
-  if (n < 0 || n > a.max_nodes) {
+  if (n > a.max_nodes) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
     return;
   }
@@ -91,7 +95,7 @@ struct StoreallCommitArgs {
   float *ST;
   const float *snap;
   const int32_t *parent, *cu_nodes, *path, *path_len;
-  int B, H, dk, dv, max_path;
+  int B, H, T, dk, dv, max_path;
   int32_t *status;
 };
 
@@ -108,6 +112,10 @@ __global__ void __launch_bounds__(kThreads) commit_storeall_kernel(StoreallCommi
   if (L == 0) return;
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
+  if (!offsets_ok(t0, n, a.T)) {
+    if (tid == 0 && chunk == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+    return;
+  }
   const int32_t *path_r = a.path + size_t(r) * a.max_path;
   if (!check_path(a.parent, path_r, t0, n, L, a.max_path)) {
     if (tid == 0 && chunk == 0 && h == 0) report(a.status, GDN_STATUS_BAD_PATH);

@@ -21,7 +21,7 @@ struct VerifyArgs {
   const uint16_t *q, *k, *v;
   const float *beta, *g;
   const int32_t *parent, *cu_nodes;
-  int B, H, dk, dv, max_nodes;
+  int B, H, T, dk, dv, max_nodes;
   float *o, *U, *G;
   int32_t *status;
 };
@@ -43,8 +43,12 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
   const int M = a.max_nodes;
+  if (!offsets_ok(t0, n, a.T)) {
+    if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+    return;
+  }
   if (n == 0) return;
-  if (n < 0 || n > M) {
+  if (n > M) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
     return;
   }

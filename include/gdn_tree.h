@@ -18,7 +18,7 @@
  *    nothing, keeps no state between calls and never synchronises the device: each call
  *    validates its scalar arguments on the host, enqueues its kernels on `stream` and
  *    returns. Results are valid once the stream has reached that point.
- *  - Layouts (T = total draft nodes = cu_nodes[B], all row-major, innermost last):
+ *  - Layouts (T = node rows allocated, T >= cu_nodes[B]; all row-major, innermost last):
  *        ST        [B][H][d_k][d_v]  fp32   committed state S^T (S is d_v x d_k)
  *        q, k      [T][H][d_k]       bf16   (passed as uint16_t bit patterns)
  *        v         [T][H][d_v]       bf16
@@ -26,14 +26,17 @@
  *        parent    [T]               int32  request-local parent index, -1 = child of the
  *                                           committed state; parent[t] < t (topological order)
  *        cu_nodes  [B+1]             int32  node offsets; request r owns nodes
- *                                           cu_nodes[r] .. cu_nodes[r+1]-1 (0..64 nodes)
+ *                                           cu_nodes[r] .. cu_nodes[r+1]-1 (0..64 nodes);
+ *                                           non-decreasing, within [0, T]
  *        o, U      [T][H][d_v]       fp32   outputs / pseudo-values
  *        G         [T][H]            fp32   cumulative log-gate over the root-to-node path
  *        path      [B][max_path]     int32  accepted path, request-local ids, root first
  *        path_len  [B]               int32  0 = keep the committed state unchanged
  *    One tree is shared by all heads of a request; each head has its own q/k/v/beta/g.
  *  - Sizes: d_k, d_v in {32, 64, 128}; 0 <= nodes per request <= max_nodes <= 64;
- *    max_path <= 64. B may be 0 (nothing is launched).
+ *    max_path <= 64. B may be 0 (nothing is launched). T is the number of node rows the
+ *    caller allocated for q, k, v, beta, g, parent, o, U and G (T >= cu_nodes[B]); with
+ *    T = 0 there are no nodes and nothing is launched.
  *  - Alignment: every array must be 16-byte aligned.
  *  - Errors: argument errors are reported by the return value before anything is launched.
  *    Data errors that only the device can see (a parent index outside [-1, t-1], a request
@@ -70,6 +73,7 @@ typedef enum gdn_status {
 #define GDN_STATUS_BAD_PATH 2u       /* accepted path is not a root-to-node chain            */
 #define GDN_STATUS_TOO_MANY_NODES 4u /* a request has more than max_nodes nodes              */
 #define GDN_STATUS_TIMEOUT 8u        /* a bounded wait on an asynchronous copy gave up       */
+#define GDN_STATUS_BAD_OFFSETS 16u   /* cu_nodes not non-decreasing inside [0, T]            */
 
 /*
  * gdn_tree_verify - outputs and pseudo-values of every draft node (tree-structured WY form).
@@ -87,26 +91,28 @@ typedef enum gdn_status {
  *   ST                 in   committed states, read only
  *   q, k, v, beta, g   in   node block
  *   parent, cu_nodes   in   tree shape
- *   B, H, d_k, d_v     in   sizes; max_nodes = an upper bound on nodes per request
+ *   B, H, T, d_k, d_v  in   sizes; max_nodes = an upper bound on nodes per request
  *   o, U, G            out  written for every node of every valid request
  *   status             out  optional device int32, GDN_STATUS_* bits OR-ed in
  */
 gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k,
                            const uint16_t *v, const float *beta, const float *g,
                            const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H,
-                           int32_t d_k, int32_t d_v, int32_t max_nodes, float *o, float *U,
-                           float *G, int32_t *status, gdn_stream_t stream);
+                           int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes, float *o,
+                           float *U, float *G, int32_t *status, gdn_stream_t stream);
 
 /*
  * gdn_tree_verify_simt - the same operation and contract as gdn_tree_verify, computed by a
- * CUDA-core (fp32 FMA) kernel instead of the tensor-core kernel. It exists as an in-run
- * cross-check of the tensor-core path; results agree within fp32 rounding.
+ * CUDA-core (fp32 FMA) kernel instead of the tensor-core kernel. gdn_tree_verify itself uses
+ * it when d_k or d_v is 32; otherwise it serves as an in-run cross-check of the tensor-core
+ * path (results agree within fp32 rounding).
  */
 gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16_t *k,
                                 const uint16_t *v, const float *beta, const float *g,
                                 const int32_t *parent, const int32_t *cu_nodes, int32_t B,
-                                int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes, float *o,
-                                float *U, float *G, int32_t *status, gdn_stream_t stream);
+                                int32_t H, int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes,
+                                float *o, float *U, float *G, int32_t *status,
+                                gdn_stream_t stream);
 
 /*
  * gdn_tree_commit - rebuild the accepted path's state in place (TreeWY page, method section:
@@ -120,8 +126,9 @@ gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16
  */
 gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint16_t *k,
                            const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
-                           const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
-                           int32_t d_v, int32_t max_path, int32_t *status, gdn_stream_t stream);
+                           const int32_t *path_len, int32_t B, int32_t H, int32_t T,
+                           int32_t d_k, int32_t d_v, int32_t max_path, int32_t *status,
+                           gdn_stream_t stream);
 
 /*
  * gdn_tree_verify_storeall - the comparison baseline the TreeWY page calls "storeall"
@@ -134,9 +141,9 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,
                                     const uint16_t *v, const float *beta, const float *g,
                                     const int32_t *parent, const int32_t *cu_nodes, int32_t B,
-                                    int32_t H, int32_t d_k, int32_t d_v, int32_t max_nodes,
-                                    float *snapshots, float *o, float *U, float *G,
-                                    int32_t *status, gdn_stream_t stream);
+                                    int32_t H, int32_t T, int32_t d_k, int32_t d_v,
+                                    int32_t max_nodes, float *snapshots, float *o, float *U,
+                                    float *G, int32_t *status, gdn_stream_t stream);
 
 /*
  * gdn_tree_commit_storeall - storeall commit: copy the stored state of the accepted path's
@@ -144,9 +151,9 @@ gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const ui
  */
 gdn_status gdn_tree_commit_storeall(float *ST, const float *snapshots, const int32_t *parent,
                                     const int32_t *cu_nodes, const int32_t *path,
-                                    const int32_t *path_len, int32_t B, int32_t H, int32_t d_k,
-                                    int32_t d_v, int32_t max_path, int32_t *status,
-                                    gdn_stream_t stream);
+                                    const int32_t *path_len, int32_t B, int32_t H, int32_t T,
+                                    int32_t d_k, int32_t d_v, int32_t max_path,
+                                    int32_t *status, gdn_stream_t stream);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);

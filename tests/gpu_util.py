@@ -31,7 +31,7 @@ def run_gpu(tb, verify: str = "wy", commit: bool = True, fill=float("nan"), max_
     mn = tb.max_nodes if max_nodes is None else max_nodes
     mp = tb.max_path if max_path is None else max_path
     args = (d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"],
-            tb.B, tb.H, tb.dk, tb.dv, mn)
+            tb.B, tb.H, tb.T, tb.dk, tb.dv, mn)
     snap = None
     if verify == "storeall":
         snap = torch.full((max(tb.T, 1), tb.H, tb.dk, tb.dv), float("nan"), device="cuda")
@@ -41,10 +41,10 @@ def run_gpu(tb, verify: str = "wy", commit: bool = True, fill=float("nan"), max_
     if commit:
         if verify == "storeall":
             gb.gdn_tree_commit_storeall(d["ST"], snap, d["parent"], d["cu_nodes"], d["path"], d["path_len"],
-                                        tb.B, tb.H, tb.dk, tb.dv, mp, out["status"])
+                                        tb.B, tb.H, tb.T, tb.dk, tb.dv, mp, out["status"])
         else:
             gb.gdn_tree_commit(d["ST"], out["U"], out["G"], d["k"], d["parent"], d["cu_nodes"], d["path"],
-                               d["path_len"], tb.B, tb.H, tb.dk, tb.dv, mp, out["status"])
+                               d["path_len"], tb.B, tb.H, tb.T, tb.dk, tb.dv, mp, out["status"])
     torch.cuda.synchronize()
     res = {"o": out["o"][:tb.T].cpu().numpy(), "U": out["U"][:tb.T].cpu().numpy(),
            "G": out["G"][:tb.T].cpu().numpy(), "ST": d["ST"].cpu().numpy(),

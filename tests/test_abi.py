@@ -23,7 +23,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_status_strings_and_version():
-    assert gb.abi_version() == 1
+    assert gb.abi_version() == 2
     for code in (gb.GDN_OK, gb.GDN_EINVAL, gb.GDN_ETOOBIG, gb.GDN_EALIGN, gb.GDN_ECUDA, gb.GDN_EARCH):
         assert gb.status_str(code).startswith("GDN_")
     assert "unknown" in gb.status_str(99)
@@ -34,11 +34,11 @@ FAKE = 0x10000  # 16-byte aligned host-side stand-in address; never dereferenced
 
 def _verify(fn, **kw):
     args = dict(ST=FAKE, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, g=FAKE, parent=FAKE, cu_nodes=FAKE, B=1, H=1,
-                d_k=32, d_v=32, max_nodes=4, o=FAKE, U=FAKE, G=FAKE, status=None)
+                T=4, d_k=32, d_v=32, max_nodes=4, o=FAKE, U=FAKE, G=FAKE, status=None)
     args.update(kw)
     return fn(args["ST"], args["q"], args["k"], args["v"], args["beta"], args["g"], args["parent"],
-              args["cu_nodes"], args["B"], args["H"], args["d_k"], args["d_v"], args["max_nodes"], args["o"],
-              args["U"], args["G"], args["status"], None)
+              args["cu_nodes"], args["B"], args["H"], args["T"], args["d_k"], args["d_v"], args["max_nodes"],
+              args["o"], args["U"], args["G"], args["status"], None)
 
 
 @pytest.mark.parametrize("name", ["gdn_tree_verify", "gdn_tree_verify_simt"])
@@ -46,7 +46,7 @@ def _verify(fn, **kw):
     (dict(d_k=48), gb.GDN_EINVAL), (dict(d_v=256), gb.GDN_EINVAL), (dict(H=0), gb.GDN_EINVAL),
     (dict(B=-1), gb.GDN_EINVAL), (dict(max_nodes=65), gb.GDN_ETOOBIG), (dict(q=None), gb.GDN_EINVAL),
     (dict(o=FAKE + 4), gb.GDN_EALIGN), (dict(status=FAKE + 8), gb.GDN_EALIGN), (dict(B=0), gb.GDN_OK),
-    (dict(B=70000), gb.GDN_EINVAL)])
+    (dict(B=70000), gb.GDN_EINVAL), (dict(T=-1), gb.GDN_EINVAL), (dict(T=0, q=None), gb.GDN_OK)])
 def test_verify_host_checks(name, kw, code):
     fn = getattr(gb.library(), name)
     assert _verify(fn, **kw) == code
@@ -57,16 +57,16 @@ def test_verify_host_checks(name, kw, code):
     (dict(U=FAKE + 2), gb.GDN_EALIGN), (dict(B=0), gb.GDN_OK)])
 def test_commit_host_checks(kw, code):
     args = dict(ST=FAKE, U=FAKE, G=FAKE, k=FAKE, parent=FAKE, cu_nodes=FAKE, path=FAKE, path_len=FAKE, B=1,
-                H=1, d_k=32, d_v=32, max_path=4, status=None)
+                H=1, T=4, d_k=32, d_v=32, max_path=4, status=None)
     args.update(kw)
     rc = gb.library().gdn_tree_commit(*[args[x] for x in ("ST", "U", "G", "k", "parent", "cu_nodes", "path",
-                                                          "path_len", "B", "H", "d_k", "d_v", "max_path",
+                                                          "path_len", "B", "H", "T", "d_k", "d_v", "max_path",
                                                           "status")], None)
     assert rc == code
 
 
 def test_binding_raises_on_error():
     with pytest.raises(gb.GdnError) as e:
-        gb.gdn_tree_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 48, 32, 4, FAKE, FAKE, FAKE,
+        gb.gdn_tree_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 48, 32, 4, FAKE, FAKE, FAKE,
                            stream=0)
     assert e.value.code == gb.GDN_EINVAL

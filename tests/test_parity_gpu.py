@@ -176,15 +176,15 @@ def test_host_argument_errors():
     tb = W.make_config(0)
     d = gd.upload(tb)
     out = gd.alloc_outputs(tb)
-    base = [d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], 1, 1, 32, 32, 3,
+    base = [d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], 1, 1, 3, 32, 32, 3,
             out["o"], out["U"], out["G"]]
     bad = list(base)
-    bad[12] = 65
+    bad[13] = 65
     with pytest.raises(gb.GdnError) as e:
         gb.gdn_tree_verify(*bad)
     assert e.value.code == gb.GDN_ETOOBIG
     bad = list(base)
-    bad[10] = 48
+    bad[11] = 48
     with pytest.raises(gb.GdnError) as e:
         gb.gdn_tree_verify(*bad)
     assert e.value.code == gb.GDN_EINVAL
@@ -198,3 +198,40 @@ def test_host_argument_errors():
     empty[8] = 0
     gb.gdn_tree_verify(*empty)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 64), (64, 128), (32, 128), (128, 32)])
+def test_mixed_key_value_widths(dk, dv):
+    rng = np.random.default_rng(dk + dv)
+    parents = [W.random_tree_parents(rng, int(n), 3, 6) for n in (5, 17, 40)]
+    paths = [W.root_path(p, W.leaves(p)[-1]) for p in parents]
+    tb = W.build_batch(rng, parents, paths, H=3, dk=dk, dv=dv)
+    for kernel in KERNELS:
+        res = run_gpu(tb, verify=kernel)
+        assert res["status"] == 0
+        check_verify(tb, res, tag=f"dk{dk}/dv{dv}/{kernel}")
+        check_commit(tb, res, tag=f"dk{dk}/dv{dv}/{kernel}")
+
+
+def test_oversized_max_nodes():
+    """Node capacity far above the actual tree sizes (the node tile spans neighbouring requests)."""
+    tb = W.make_config(2, batch=64, heads=4)
+    padded = np.full((tb.B, 64), -1, np.int32)  # path rows are max_path apart
+    padded[:, :tb.path.shape[1]] = tb.path
+    tb.path = padded
+    res = run_gpu(tb, verify="wy", max_nodes=64)
+    assert res["status"] == 0
+    check_verify(tb, res, tag="config2/max_nodes64")
+    check_commit(tb, res, tag="config2/max_nodes64")
+
+
+@pytest.mark.parametrize("kernel", KERNELS + ["storeall"])
+def test_bad_offsets_reported(kernel):
+    tb = W.make_random_batch(seed=11, B=3, H=2, d=64, n_range=(4, 6))
+    T = tb.T
+    tb.cu_nodes[2] = T + 5  # request 1 runs past the allocated rows, request 2 has negative size
+    tb.path_len[:] = 0
+    res = run_gpu(tb, verify=kernel, commit=False)
+    assert res["status"] & gb.STATUS_BAD_OFFSETS
+    r0 = slice(0, tb.cu_nodes[1])
+    assert np.all(np.isfinite(res["o"][r0]))
