@@ -13,6 +13,7 @@
 #include "commit.cuh"
 #include "storeall.cuh"
 #include "verify_simt.cuh"
+#include "verify_stream.cuh"
 #include "verify_tc.cuh"
 
 using namespace gdn;
@@ -123,6 +124,13 @@ gdn_status launch_verify_simt(const VerifyArgs &a, cudaStream_t stream) {
   return launch_status();
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
 template <int DK, int DV>
 gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
   const int Np = ((a.max_nodes < 1 ? 1 : a.max_nodes) + 15) / 16 * 16;
@@ -131,12 +139,52 @@ gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
       !encode_rows(&tq, a.q, DK, a.H, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_rows(&tv, a.v, DV, a.H, a.T, DV, Np, CU_TENSOR_MAP_SWIZZLE_NONE))
     return GDN_ECUDA;
-  const size_t smem = tc_smem_bytes(DK, DV, Np);
+  int dev = 0, optin = 0;
+  cudaFuncAttributes fa{};
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, verify_tc_kernel<DK, DV>) != cudaSuccess)
+    return GDN_ECUDA;
+  // deepest state ring that fits next to the node stages (1 KiB slack aligns the base)
+  const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024;
+  int R = kMaxRing;
+  while (R > 2 && (long long)tc_layout(DK, DV, Np, R).total > room) --R;
+  const TcLayout lay = tc_layout(DK, DV, Np, R);
+  if ((long long)lay.total > room) return GDN_ECUDA;
+  // at least ~half an SM's shared memory, so a second CTA never waits on this one's tensor memory
+  size_t smem = size_t(lay.total) + 1024;
+  if (smem < 120u * 1024u) smem = 120u * 1024u;
   if (cudaFuncSetAttribute(verify_tc_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return GDN_ECUDA;
+  const long long pairs = (long long)a.B * a.H;
+  const int sms = sm_count();
+  if (sms <= 0) return GDN_ECUDA;
+  const unsigned grid = unsigned(pairs < sms ? pairs : sms);
+  verify_tc_kernel<DK, DV><<<grid, kTcThreads, smem, stream>>>(tk, tq, tv, a, lay);
+  return launch_status();
+}
+
+template <int DK, int DV, int NMAX>
+gdn_status launch_verify_stream(const VerifyArgs &a, cudaStream_t stream) {
   const long long blocks = (long long)a.B * a.H;
-  verify_tc_kernel<DK, DV><<<unsigned(blocks), kThreads, smem, stream>>>(tk, tq, tv, a, Np);
+  verify_stream_kernel<DK, DV, NMAX><<<unsigned(blocks), DV / 2, 0, stream>>>(a);
+  return launch_status();
+}
+
+template <int DK, int DV>
+gdn_status launch_verify_stream_n(const VerifyArgs &a, cudaStream_t stream) {
+  return a.max_nodes <= 4 ? launch_verify_stream<DK, DV, 4>(a, stream) : launch_verify_stream<DK, DV, 8>(a, stream);
+}
+
+template <int DK, int DV>
+gdn_status launch_commit(const CommitArgs &a, cudaStream_t stream) {
+  const size_t smem = commit_smem_bytes(a.max_path, DK, DV);
+  if (cudaFuncSetAttribute(commit_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+      cudaSuccess)
+    return GDN_ECUDA;
+  const long long blocks = (long long)a.B * a.H;
+  commit_kernel<DK, DV><<<unsigned(blocks), kThreads, smem, stream>>>(a);
   return launch_status();
 }
 
@@ -192,13 +240,23 @@ gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k
   gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
                                     max_nodes, o, U, G, status);
   if (st != GDN_OK || B == 0 || T == 0) return st;
-  if (d_k == 32 || d_v == 32)
+  if (d_v == 32 || (d_k == 32 && max_nodes > kStreamMaxNodes))
     return gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o,
                                 U, G, status, stream);
   if ((st = check_device()) != GDN_OK) return st;
   if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
   VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (max_nodes <= kStreamMaxNodes) {  // small trees: CUDA-core streaming kernel
+    switch (d_k * 1000 + d_v) {
+      case 32064: return launch_verify_stream_n<32, 64>(a, s);
+      case 32128: return launch_verify_stream_n<32, 128>(a, s);
+      case 64064: return launch_verify_stream_n<64, 64>(a, s);
+      case 64128: return launch_verify_stream_n<64, 128>(a, s);
+      case 128064: return launch_verify_stream_n<128, 64>(a, s);
+      default: return launch_verify_stream_n<128, 128>(a, s);
+    }
+  }
   if (d_k == 128) return d_v == 128 ? launch_verify_tc<128, 128>(a, s) : launch_verify_tc<128, 64>(a, s);
   return d_v == 128 ? launch_verify_tc<64, 128>(a, s) : launch_verify_tc<64, 64>(a, s);
 }
@@ -211,16 +269,20 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
                                     max_path, status);
   if (st != GDN_OK || B == 0) return st;
   if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
   CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
-  const size_t smem = commit_smem_bytes(max_path, d_k, d_v);
-  if (cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-      cudaSuccess)
-    return GDN_ECUDA;
-  const long long nchunk = d_k / commit_rows_per_cta(d_k, d_v);
-  const long long blocks = (long long)B * H * nchunk;
-  if (blocks > 0x7fffffffLL) return GDN_EINVAL;
-  commit_kernel<<<unsigned(blocks), kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-  return launch_status();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d_k * 1000 + d_v) {
+    case 32032: return launch_commit<32, 32>(a, s);
+    case 32064: return launch_commit<32, 64>(a, s);
+    case 32128: return launch_commit<32, 128>(a, s);
+    case 64032: return launch_commit<64, 32>(a, s);
+    case 64064: return launch_commit<64, 64>(a, s);
+    case 64128: return launch_commit<64, 128>(a, s);
+    case 128032: return launch_commit<128, 32>(a, s);
+    case 128064: return launch_commit<128, 64>(a, s);
+    default: return launch_commit<128, 128>(a, s);
+  }
 }
 
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,

@@ -1,14 +1,21 @@
 // Commit: rebuild only the accepted path's state, in place (TreeWY, method section: only the
-// accepted path's pseudo-values are combined into the next committed state).
+// accepted path's pseudo-values are combined into the next committed state; novelty section:
+// exactly one full state is rebuilt).
 //
 // With l the accepted path's last node, for every (request, head):
 //   ST[kk][c] <- exp(G_l) ST[kk][c] + sum_{j on path} (exp(G_l - G_j) k_j[kk]) u_j[c]
-// Each CTA streams one 16 KiB slab of one state (whole rows of d_v): it issues its slab loads
-// first, checks the path and stages the path's coefficients while they are in flight, then
-// writes each element once. Pure HBM streaming: 8 bytes of state traffic per element.
+//
+// One CTA per (request, head). Thread 0 reads the path length and node offsets and, for a
+// non-empty path, starts one bulk copy (cp.async.bulk, mbarrier completion) of the whole
+// d_k x d_v state into shared memory. While the copy is in flight the CTA checks the path and
+// stages the path's coefficients (exp(G_l - G_j) k_j and u_j). Each thread then owns one fixed
+// group of four state columns, keeps the path's u_j for those columns in registers as it goes,
+// accumulates its float4s and writes each one to HBM once with a streaming store. State
+// traffic: one read and one write per element, nothing else.
 #pragma once
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gdn {
 
@@ -21,83 +28,113 @@ struct CommitArgs {
   int32_t *status;
 };
 
-constexpr int kCommitVec = 4;  // float4 per thread per slab
-
-__host__ __device__ inline int commit_rows_per_cta(int dk, int dv) {
-  int rows = (kThreads * kCommitVec * 4) / dv;  // 1024 float4 per CTA
-  return rows < dk ? rows : dk;
-}
+constexpr uint64_t kCommitWaitNs = 1000000000ull;  // 1 s bound on the state copy
 
 __host__ __device__ inline size_t commit_smem_bytes(int max_path, int dk, int dv) {
-  return sizeof(float) * size_t(max_path) * (commit_rows_per_cta(dk, dv) + dv);
+  return size_t(dk) * dv * 4                       // the state
+         + size_t(max_path) * (dk + dv) * 4;       // exp(G_l - G_j) k_j and u_j per path entry
 }
 
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
-  extern __shared__ __align__(16) float dyn[];
-  const int tid = threadIdx.x;
-  const int KR = commit_rows_per_cta(a.dk, a.dv);
-  const int nchunk = a.dk / KR;
-  const int chunk = blockIdx.x % nchunk;
-  const int pair = blockIdx.x / nchunk;
-  const int h = pair % a.H, r = pair / a.H;
-  const int L = a.path_len[r];
-  if (L == 0) return;  // keep the committed state
-  const int t0 = a.cu_nodes[r];
-  const int n = a.cu_nodes[r + 1] - t0;
-  if (!offsets_ok(t0, n, a.T)) {
-    if (tid == 0 && blockIdx.x % (nchunk * a.H) == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
-    return;
-  }
-  const int dv4 = a.dv >> 2;
-  const int nf = KR * dv4;
-  float4 *slab = reinterpret_cast<float4 *>(a.ST + ((size_t(r) * a.H + h) * a.dk + size_t(chunk) * KR) * a.dv);
+  constexpr int DV4 = DV / 4;
+  constexpr int J = DK * DV4 / kThreads;  // float4 of the state per thread
+  constexpr int ROWSTEP = kThreads / DV4;  // state rows between a thread's float4s
+  static_assert(J >= 1 && (DK * DV4) % kThreads == 0, "state must tile the block");
+  constexpr uint32_t kStateBytes = DK * DV * 4;
+  constexpr uint32_t kPiece = kStateBytes < 16384u ? kStateBytes : 16384u;
 
-  // issue the slab loads before anything else so they are in flight during the set-up
-  float4 x[kCommitVec];
+  extern __shared__ __align__(128) uint8_t commit_dyn[];
+  float4 *xs = reinterpret_cast<float4 *>(commit_dyn);
+  float *kw = reinterpret_cast<float *>(commit_dyn + kStateBytes);          // [max_path][DK]
+  float4 *us = reinterpret_cast<float4 *>(kw + size_t(a.max_path) * DK);  // [max_path][DV4]
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_info[3];  // L, t0, n
+
+  const int tid = threadIdx.x;
+  const int pair = blockIdx.x;
+  const int h = pair % a.H, r = pair / a.H;
+  float *ST = a.ST + size_t(pair) * DK * DV;
+
+  if (tid == 0) {
+    const int L = a.path_len[r];
+    const int t0 = a.cu_nodes[r];
+    const int n = a.cu_nodes[r + 1] - t0;
+    int go = L != 0;
+    if (go && !offsets_ok(t0, n, a.T)) {
+      if (h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+      go = 0;
+    }
+    if (go && (L < 0 || L > n || L > a.max_path)) {
+      if (h == 0) report(a.status, GDN_STATUS_BAD_PATH);
+      go = 0;
+    }
+    s_info[0] = go ? L : 0;
+    s_info[1] = t0;
+    s_info[2] = n;
+    if (go) {
+      ptx::mbar_init(&bar, 1);
+      ptx::fence_mbar_init();
+      ptx::mbar_arrive_expect_tx(&bar, kStateBytes);
 #pragma unroll
-  for (int j = 0; j < kCommitVec; ++j) {
-    const int f = tid + j * kThreads;
-    if (f < nf) x[j] = __ldcs(slab + f);
-  }
-  const int32_t *path_r = a.path + size_t(r) * a.max_path;
-  if (!check_path(a.parent, path_r, t0, n, L, a.max_path)) {
-    if (tid == 0 && chunk == 0 && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
-    return;
-  }
-  float *kw = dyn;                        // [L][KR]   exp(G_l - G_j) k_j[row]
-  float *us = dyn + size_t(a.max_path) * KR;  // [L][dv]   u_j
-  const int l = path_r[L - 1];
-  const float Gl = a.G[size_t(t0 + l) * a.H + h];
-  for (int i = tid; i < L * KR; i += kThreads) {
-    const int s = i / KR, row = i % KR;
-    const size_t th = size_t(t0 + path_r[s]) * a.H + h;
-    kw[i] = expf(Gl - a.G[th]) * bf16_to_f32(a.k[th * a.dk + size_t(chunk) * KR + row]);
-  }
-  for (int i = tid; i < L * dv4; i += kThreads) {
-    const int s = i / dv4, c4 = i % dv4;
-    const size_t th = size_t(t0 + path_r[s]) * a.H + h;
-    reinterpret_cast<float4 *>(us)[i] = reinterpret_cast<const float4 *>(a.U + th * a.dv)[c4];
-  }
-  __syncthreads();
-  const float decay = expf(Gl);
-#pragma unroll
-  for (int j = 0; j < kCommitVec; ++j) {
-    const int f = tid + j * kThreads;
-    if (f < nf) {
-      const int row = f / dv4, c4 = f % dv4;
-      float4 y = x[j];
-      y.x *= decay; y.y *= decay; y.z *= decay; y.w *= decay;
-      for (int s = 0; s < L; ++s) {
-        const float w = kw[s * KR + row];
-        const float4 u = reinterpret_cast<const float4 *>(us)[s * dv4 + c4];
-        y.x = fmaf(w, u.x, y.x);
-        y.y = fmaf(w, u.y, y.y);
-        y.z = fmaf(w, u.z, y.z);
-        y.w = fmaf(w, u.w, y.w);
-      }
-      __stcs(slab + f, y);
+      for (uint32_t off = 0; off < kStateBytes; off += kPiece)
+        ptx::bulk_load(commit_dyn + off, reinterpret_cast<const uint8_t *>(ST) + off, kPiece, &bar);
     }
   }
+  __syncthreads();
+  const int L = s_info[0];
+  if (L == 0) return;  // empty path (keep the state) or a rejected request: no copy in flight
+  const int t0 = s_info[1], n = s_info[2];
+
+  // path check and coefficient staging overlap the state copy
+  const int32_t *path_r = a.path + size_t(r) * a.max_path;
+  const bool path_ok = check_path(a.parent, path_r, t0, n, L, a.max_path);
+  if (path_ok) {
+    const int l = path_r[L - 1];
+    const float Gl = a.G[size_t(t0 + l) * a.H + h];
+    for (int i = tid; i < L * DK; i += kThreads) {
+      const int s = i / DK, row = i % DK;
+      const size_t th = size_t(t0 + path_r[s]) * a.H + h;
+      kw[i] = expf(Gl - a.G[th]) * bf16_to_f32(a.k[th * DK + row]);
+    }
+    for (int i = tid; i < L * DV4; i += kThreads) {
+      const int s = i / DV4, c4 = i % DV4;
+      const size_t th = size_t(t0 + path_r[s]) * a.H + h;
+      us[i] = reinterpret_cast<const float4 *>(a.U + th * DV)[c4];
+    }
+  }
+  __syncthreads();
+  const bool landed = ptx::mbar_wait(&bar, 0, kCommitWaitNs);
+  if (!path_ok || !__syncthreads_and(landed)) {
+    if (tid == 0 && !path_ok && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
+    if (tid == 0 && path_ok) report(a.status, GDN_STATUS_TIMEOUT);
+    if (path_ok) ptx::mbar_wait(&bar, 0, kCommitWaitNs);  // let the copy land before leaving
+    return;
+  }
+
+  const int c4 = tid % DV4, row0 = tid / DV4;
+  const float decay = expf(a.G[size_t(t0 + path_r[L - 1]) * a.H + h]);
+  float4 y[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const float4 x = xs[tid + j * kThreads];
+    y[j] = make_float4(decay * x.x, decay * x.y, decay * x.z, decay * x.w);
+  }
+  for (int s = 0; s < L; ++s) {
+    const float4 u = us[s * DV4 + c4];
+    const float *w = kw + s * DK + row0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float wv = w[j * ROWSTEP];
+      y[j].x = fmaf(wv, u.x, y[j].x);
+      y[j].y = fmaf(wv, u.y, y[j].y);
+      y[j].z = fmaf(wv, u.z, y[j].z);
+      y[j].w = fmaf(wv, u.w, y[j].w);
+    }
+  }
+  float4 *dst = reinterpret_cast<float4 *>(ST);
+#pragma unroll
+  for (int j = 0; j < J; ++j) __stcs(dst + tid + j * kThreads, y[j]);
 }
 
 }  // namespace gdn

@@ -1,0 +1,217 @@
+// CUDA-core streaming tree verify for small trees (at most NMAX <= 8 nodes per request): the
+// tree-structured WY form of the gated delta rule (TreeWY, method section) with every per-node
+// quantity held in registers.
+//
+// One CTA per (request, head), DV/2 threads; thread i owns state columns 2i and 2i+1. The CTA
+// issues its first state rows before anything else, then stages the node block (keys and
+// queries widened to fp32) in shared memory and analyses the tree while those loads are in
+// flight. The fp32 state then streams from HBM exactly once, kStreamPF rows ahead of use, and
+// every row updates the thread's 2 x 2*NMAX projection accumulators
+//     KS_t = S_0 k_t,   QS_t = S_0 q_t            (fp32 FMA, fp32 accumulate)
+// Per node (registers, loops fully unrolled over the NMAX slots, ancestor tests uniform across
+// the CTA):
+//     R_t = b_t (v_t - gamma_t KS_t),  u_t = R_t - sum_{j strict ancestor} A[t,j] u_j
+//     o_t = gamma_t QS_t + sum_{j ancestor or t} P[t,j] u_j
+// with A[t,j] = b_t exp(G_t - G_j) k_t.k_j and P[t,j] = exp(G_t - G_j) q_t.k_j from warp-split
+// dot products. At N <= 8 the 4 N d_k d_v FMAs per pair stay below the time the pair's state
+// takes to arrive from HBM, so the kernel is bandwidth-bound without tensor cores or any
+// shared-memory round trip of the state.
+#pragma once
+
+#include "common.cuh"
+#include "verify_simt.cuh"
+
+namespace gdn {
+
+constexpr int kStreamPF = 16;       // state rows in flight per thread
+constexpr int kStreamMaxNodes = 8;  // largest tree the streaming kernel takes
+
+__device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
+  return make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
+}
+
+template <int DK, int DV, int NMAX>
+__global__ void __launch_bounds__(DV / 2) verify_stream_kernel(VerifyArgs a) {
+  constexpr int NT = DV / 2;    // threads
+  constexpr int NW = NT / 32;   // warps
+  constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
+  constexpr int DV2 = DV / 2;   // float2 per state row
+  static_assert(NMAX <= 8 && DK % kStreamPF == 0 && NT % 32 == 0, "shape");
+  __shared__ __align__(16) float Xs[NX][DK];
+  __shared__ float Ac[NMAX][NMAX], Pc[NMAX][NMAX];
+  __shared__ float G_s[NMAX], gam_s[NMAX], beta_s[NMAX], g_s[NMAX];
+  __shared__ int par_s[NMAX];
+  __shared__ uint32_t anc_s[NMAX];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int pair = blockIdx.x, h = pair % a.H, r = pair / a.H;
+  const float2 *st = reinterpret_cast<const float2 *>(a.ST + size_t(pair) * DK * DV) + tid;
+
+  // 1) the first state rows go out before any dependent load
+  float2 s[kStreamPF];
+#pragma unroll
+  for (int i = 0; i < kStreamPF; ++i) s[i] = __ldcs(st + i * DV2);
+
+  // 2) request bounds and checks
+  const int t0 = a.cu_nodes[r];
+  const int n = a.cu_nodes[r + 1] - t0;
+  if (!offsets_ok(t0, n, a.T)) {
+    if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+    return;
+  }
+  if (n == 0) return;
+  if (n > a.max_nodes || n > NMAX) {
+    if (tid == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
+    return;
+  }
+  const int H = a.H;
+
+  // 3) node block (fp32, rows >= n zero), this thread's v pairs, tree inputs
+  for (int i = tid; i < NX * DK / 4; i += NT) {
+    const int row = i / (DK / 4), c4 = i % (DK / 4);
+    const int t = row < NMAX ? row : row - NMAX;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < n) {
+      const uint16_t *src = (row < NMAX ? a.k : a.q) + (size_t(t0 + t) * H + h) * DK + 4 * c4;
+      const uint2 w = *reinterpret_cast<const uint2 *>(src);
+      const float2 lo = bf16x2_to_f32(w.x), hi = bf16x2_to_f32(w.y);
+      x = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    *reinterpret_cast<float4 *>(&Xs[row][4 * c4]) = x;
+  }
+  uint32_t vb[NMAX];
+#pragma unroll
+  for (int t = 0; t < NMAX; ++t)
+    vb[t] = t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * tid) : 0u;
+  int bad = 0;
+  if (tid < n) {
+    const int p = a.parent[t0 + tid];
+    bad = (p < -1 || p >= tid);
+    par_s[tid] = p;
+    g_s[tid] = a.g[size_t(t0 + tid) * H + h];
+    beta_s[tid] = a.beta[size_t(t0 + tid) * H + h];
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
+    return;
+  }
+  if (tid < n) {
+    // parent indices strictly decrease along the walk, so it ends within tid + 1 steps
+    uint32_t m = 1u << tid;
+    float Gs = g_s[tid];
+    for (int x = par_s[tid]; x >= 0; x = par_s[x]) {
+      m |= 1u << x;
+      Gs += g_s[x];
+    }
+    anc_s[tid] = m;
+    G_s[tid] = Gs;
+    gam_s[tid] = expf(Gs);
+  }
+  __syncthreads();
+
+  // 4) stream the state once: KS (rows 0..NMAX-1) and QS (rows NMAX..) for two columns
+  float2 acc[NX];
+#pragma unroll
+  for (int t = 0; t < NX; ++t) acc[t] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int k0 = 0; k0 < DK; k0 += kStreamPF) {
+    float2 nx[kStreamPF];
+    if (k0 + kStreamPF < DK) {
+#pragma unroll
+      for (int i = 0; i < kStreamPF; ++i) nx[i] = __ldcs(st + (k0 + kStreamPF + i) * DV2);
+    }
+#pragma unroll
+    for (int g4 = 0; g4 < kStreamPF; g4 += 4) {
+#pragma unroll
+      for (int t = 0; t < NX; ++t) {
+        const float4 x = *reinterpret_cast<const float4 *>(&Xs[t][k0 + g4]);
+        acc[t].x = fmaf(x.x, s[g4].x, acc[t].x);
+        acc[t].y = fmaf(x.x, s[g4].y, acc[t].y);
+        acc[t].x = fmaf(x.y, s[g4 + 1].x, acc[t].x);
+        acc[t].y = fmaf(x.y, s[g4 + 1].y, acc[t].y);
+        acc[t].x = fmaf(x.z, s[g4 + 2].x, acc[t].x);
+        acc[t].y = fmaf(x.z, s[g4 + 2].y, acc[t].y);
+        acc[t].x = fmaf(x.w, s[g4 + 3].x, acc[t].x);
+        acc[t].y = fmaf(x.w, s[g4 + 3].y, acc[t].y);
+      }
+    }
+    if (k0 + kStreamPF < DK) {
+#pragma unroll
+      for (int i = 0; i < kStreamPF; ++i) s[i] = nx[i];
+    }
+  }
+
+  // 5) masked, gated Gram entries: one warp per (t, j) entry, lanes split d_k
+  {
+    int e = 0;
+    for (int t = 0; t < n; ++t) {
+      uint32_t m = anc_s[t];
+      while (m) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1;
+        if (e++ % NW != warp) continue;
+        float kk = 0.f, qk = 0.f;
+#pragma unroll
+        for (int c = lane; c < DK; c += 32) {
+          kk = fmaf(Xs[t][c], Xs[j][c], kk);
+          qk = fmaf(Xs[NMAX + t][c], Xs[j][c], qk);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          kk += __shfl_xor_sync(0xffffffffu, kk, off);
+          qk += __shfl_xor_sync(0xffffffffu, qk, off);
+        }
+        if (lane == 0) {
+          const float w = expf(G_s[t] - G_s[j]);
+          Ac[t][j] = beta_s[t] * w * kk;
+          Pc[t][j] = w * qk;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // 6) solve and outputs in registers
+  float2 u[NMAX];
+#pragma unroll
+  for (int t = 0; t < NMAX; ++t) {
+    u[t] = make_float2(0.f, 0.f);
+    if (t < n) {
+      const float2 vv = bf16x2_to_f32(vb[t]);
+      const float gm = gam_s[t], b = beta_s[t];
+      float2 uu = make_float2(b * (vv.x - gm * acc[t].x), b * (vv.y - gm * acc[t].y));
+      const uint32_t m = anc_s[t];
+#pragma unroll
+      for (int j = 0; j < t; ++j) {
+        if ((m >> j) & 1u) {
+          const float c = Ac[t][j];
+          uu.x = fmaf(-c, u[j].x, uu.x);
+          uu.y = fmaf(-c, u[j].y, uu.y);
+        }
+      }
+      u[t] = uu;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NMAX; ++t) {
+    if (t < n) {
+      const float gm = gam_s[t];
+      float2 o = make_float2(gm * acc[NMAX + t].x, gm * acc[NMAX + t].y);
+      const uint32_t m = anc_s[t];
+#pragma unroll
+      for (int j = 0; j <= t; ++j) {
+        if ((m >> j) & 1u) {
+          const float c = Pc[t][j];
+          o.x = fmaf(c, u[j].x, o.x);
+          o.y = fmaf(c, u[j].y, o.y);
+        }
+      }
+      const size_t row = (size_t(t0 + t) * H + h) * DV2 + tid;
+      __stcs(reinterpret_cast<float2 *>(a.o) + row, o);
+      __stcs(reinterpret_cast<float2 *>(a.U) + row, u[t]);
+    }
+  }
+  if (tid < n) a.G[size_t(t0 + tid) * H + h] = G_s[tid];
+}
+
+}  // namespace gdn

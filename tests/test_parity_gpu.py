@@ -3,8 +3,9 @@
 Covers all five synthetic configurations at their full sizes (sampled (request, head) pairs
 for the oracle where the whole batch would take it too long), tiny and ragged random trees in
 random topological orders, empty requests, the deepest (chain of 64) and widest (star of 64)
-trees, forests, both verify kernels (tensor-core WY and CUDA-core WY), the store-all
-comparison kernels, and the device-side error reporting.
+trees, forests, every verify kernel (gdn_tree_verify takes the register-resident streaming
+kernel when max_nodes <= 8 and the tensor-core kernel above that; gdn_tree_verify_simt is the
+CUDA-core kernel), the store-all comparison kernels, and the device-side error reporting.
 """
 
 import numpy as np
@@ -30,10 +31,11 @@ def test_config0_full(kernel):
     check_commit(tb, res, tag=f"config0/{kernel}")
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_config1_full_size_sampled(kernel):
+@pytest.mark.parametrize("kernel,max_nodes", [("wy", None), ("wy", 16), ("simt", None)])
+def test_config1_full_size_sampled(kernel, max_nodes):
+    """Chain of 4: the streaming kernel (max_nodes = 4) and the tensor-core kernel (16)."""
     tb = W.make_config(1)  # B=256, H=32, d=128, chain of 4
-    res = run_gpu(tb, verify=kernel)
+    res = run_gpu(tb, verify=kernel, max_nodes=max_nodes)
     assert res["status"] == 0
     assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["U"]))
     pairs = sample_pairs(tb, 96, seed=1)
@@ -42,10 +44,10 @@ def test_config1_full_size_sampled(kernel):
 
 
 @pytest.mark.parametrize("batch", [1, 64])
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_config2(batch, kernel):
+@pytest.mark.parametrize("kernel,max_nodes", [("wy", None), ("wy", 32), ("simt", None)])
+def test_config2(batch, kernel, max_nodes):
     tb = W.make_config(2, batch=batch)
-    res = run_gpu(tb, verify=kernel)
+    res = run_gpu(tb, verify=kernel, max_nodes=max_nodes)
     assert res["status"] == 0
     pairs = None if batch == 1 else sample_pairs(tb, 96, seed=2)
     check_verify(tb, res, pairs, tag=f"config2/B{batch}/{kernel}")
@@ -235,3 +237,52 @@ def test_bad_offsets_reported(kernel):
     assert res["status"] & gb.STATUS_BAD_OFFSETS
     r0 = slice(0, tb.cu_nodes[1])
     assert np.all(np.isfinite(res["o"][r0]))
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (64, 128), (128, 64), (32, 128), (32, 64)])
+@pytest.mark.parametrize("nmax", [4, 8])
+def test_small_trees_streaming_kernel(dk, dv, nmax):
+    """Trees of at most 8 nodes (forests, random topological orders, empty requests) take the
+    register-resident streaming kernel; both of its node capacities (4 and 8)."""
+    rng = np.random.default_rng(1000 + dk + dv + nmax)
+    parents, paths = [], []
+    for r in range(13):
+        if r % 5 == 4:
+            parents.append(np.zeros(0, np.int32))
+            paths.append([])
+            continue
+        n = int(rng.integers(1, nmax + 1))
+        p = W.random_tree_parents(rng, n, fanout_max=3, depth_max=7)
+        if r % 3 == 1 and n > 2:  # a forest: cut one edge
+            p = p.copy()
+            p[int(rng.integers(1, n))] = -1
+        p, _ = W.random_topological_relabel(rng, p)
+        parents.append(p)
+        leaf = W.leaves(p)[int(rng.integers(len(W.leaves(p))))]
+        full = W.root_path(p, leaf)
+        paths.append(full[:int(rng.integers(0, len(full) + 1))])
+    tb = W.build_batch(rng, parents, paths, H=3, dk=dk, dv=dv)
+    res = run_gpu(tb, verify="wy", max_nodes=nmax)
+    assert res["status"] == 0
+    check_verify(tb, res, tag=f"stream/dk{dk}/dv{dv}/n{nmax}")
+    check_commit(tb, res, tag=f"stream/dk{dk}/dv{dv}/n{nmax}")
+
+
+def test_small_trees_streaming_kernel_errors():
+    """Bad parent, too many nodes and bad offsets on the streaming path: reported, and only the
+    affected request is skipped."""
+    tb = W.make_random_batch(seed=12, B=4, H=2, d=128, n_range=(3, 6))
+    tb.parent[tb.cu_nodes[1] + 2] = 2  # node 2 of request 1 names itself
+    tb.path_len[:] = 0
+    res = run_gpu(tb, verify="wy", commit=False, max_nodes=6)
+    assert res["status"] & gb.STATUS_BAD_TREE
+    r1 = slice(tb.cu_nodes[1], tb.cu_nodes[2])
+    assert np.all(np.isnan(res["o"][r1]))
+    for r in (0, 2, 3):
+        rs = slice(tb.cu_nodes[r], tb.cu_nodes[r + 1])
+        assert np.all(np.isfinite(res["o"][rs]))
+    tb2 = W.make_random_batch(seed=13, B=3, H=2, d=128, n_range=(5, 7))
+    tb2.path_len[:] = 0
+    res = run_gpu(tb2, verify="wy", commit=False, max_nodes=4)
+    assert res["status"] & gb.STATUS_TOO_MANY_NODES
+    assert np.all(np.isnan(res["o"]))
