@@ -7,23 +7,28 @@
 //   Gram         D2[m][j] = sum_k X[m][k] K[j][k]   -> k_t.k_j (m = t), q_t.k_j (m = Np + t)
 //   masks        A[t,j] = b_t exp(G_t - G_j) k_t.k_j   (j a strict ancestor of t)
 //                P[t,j] = exp(G_t - G_j) q_t.k_j       (j an ancestor of t, or t)
-//   solve        (I + A) U = R,  R_t = b_t (v_t - gamma_t KS_t)   one state column per thread
-//   outputs      o_t = gamma_t QS_t + sum_j P[t,j] u_j
+//   inverse      T = (I + A)^-1 and W = P T. Both keep the ancestor pattern, so row t has one
+//                entry per node of t's root-to-node path; one thread per row sweeps it in
+//                registers (no chain through other rows for T, one barrier before W)
+//   solve+out    D3[v][n] = sum_j R[j][v] [T ; W][n][j],  R_t = b_t (v_t - gamma_t KS_t):
+//                u_t = D3[:, t], o_t = gamma_t QS_t + D3[:, Np + t]. tcgen05.mma with R and
+//                [T ; W] split into bf16 hi + lo (three products), fp32 accumulate in TMEM
 //
-// Warp roles (512 threads):
+// Warp roles (640 threads):
 //   warp 0       state producer: 1-D bulk copies (cp.async.bulk) of 64-row fp32 chunks of the
 //                state into a ring of 32 KiB shared-memory slots
 //   warp 1       node producer: TMA (cp.async.bulk.tensor) of the K and Q rows straight into the
-//                128-byte-swizzled K-major UMMA operand layout, and of the v rows, double-buffered
-//   warp 2       MMA issuer (one thread) and tensor-memory owner: tcgen05.mma kind::f16, fp32
-//                accumulators in TMEM, two buffers of 256 columns so the epilogue of one pair
-//                overlaps the MMAs of the next
-//   warp 3       tree analysis: parent check, 64-bit ancestor masks, cumulative log-gates and the
-//                packed offsets of the ancestor coefficients, double-buffered
-//   warps 4-7    epilogue: Gram rows from TMEM -> masked, gated coefficients in shared memory;
-//                then one state column per thread (TMEM lane = column): R, forward substitution,
-//                outputs, coalesced stores of o and U
-//   warps 8-15   splitters: each fp32 chunk is split in place into bf16 hi + lo parts
+//                128-byte-swizzled K-major UMMA operand layout (one buffer, refilled once the
+//                previous pair's MMAs are done), and of the v rows (one buffer, refilled once
+//                the previous pair's R is formed)
+//   warp 2       MMA issuer for the projections and the Gram (one thread) and tensor-memory
+//                owner: tcgen05.mma kind::f16, fp32 accumulators in TMEM, two buffers of 256
+//                columns so the epilogue of one pair overlaps the MMAs of the next
+//   warp 3       tree analysis: parent check, 64-bit ancestor masks, cumulative log-gates, depths
+//                and each node's root-to-node path table, double-buffered
+//   warps 4-11   epilogue: Gram rows from TMEM -> masked, gated path coefficients; T and W; the
+//                dense [T ; W] and R operands; the solve/output MMA; o and U stores
+//   warps 12-19  splitters: each fp32 chunk is split in place into bf16 hi + lo parts
 //                (S = hi + lo + O(2^-17 |S|)) written as the K-major, 128-byte-swizzled UMMA A
 //                operand; two MMAs per K slice (hi, lo) give fp32-accurate products against
 //                the exact bf16 q / k
@@ -39,7 +44,7 @@
 namespace gdn {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s bound on every wait
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 640;
 constexpr int kChunkRows = 64;            // state rows (along d_k) per ring slot
 constexpr uint32_t kSlotBytes = 32768;    // fp32 chunk, then bf16 hi (16 KiB) + lo (16 KiB)
 constexpr uint32_t kRegionBytes = 16384;  // 128 rows x 128 B: one 64-wide K region of an operand
@@ -54,17 +59,23 @@ enum : int {
   kWarpMma = 2,
   kWarpTree = 3,
   kWarpEpi = 4,
-  kEpiThreads = 128,
-  kWarpSplit = 8,
+  kEpiThreads = 256,
+  kWarpSplit = 12,
   kSplitThreads = 256,
 };
 
 enum : int { kBarSplit = 1, kBarEpi = 2 };  // named barriers (0 is __syncthreads)
 
 // Shared-memory carve-up (byte offsets from a 1024-byte-aligned base).
+//   ring   R slots of 32 KiB: fp32 state chunks, split in place to the bf16 hi / lo A operand
+//   x      the [K ; Q] B operand of the projections and the A / B operands of the Gram
+//   v      v rows (bf16)
+//   aop    R^T as the A operand of the solve/output MMA (hi, lo: 128 rows x 128 B each); before
+//          R exists the same bytes hold the packed path coefficients A, P and T (fp32)
+//   bop    [T ; W] as its B operand (hi, lo: 2 Np rows x 128 B each)
 struct TcLayout {
-  int Np, R, u_in_x;
-  uint32_t ring, x, v, ap, u, total;
+  int Np, R;
+  uint32_t ring, x, v, aop, bop, ca, cp, ct, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -73,19 +84,21 @@ __host__ __device__ inline TcLayout tc_layout(int DK, int DV, int Np, int R) {
   TcLayout L{};
   L.Np = Np;
   L.R = R;
+  const uint32_t ncoef = align_up(uint32_t(Np) * (Np + 1) / 2 * 4, 128);  // one packed coefficient array
   uint32_t off = 0;
   L.ring = off;
   off += uint32_t(R) * kSlotBytes;
   L.x = off;
-  off += 2u * uint32_t(DK / 64) * kRegionBytes;
+  off += uint32_t(DK / 64) * kRegionBytes;
   L.v = off;
-  off = align_up(off + 2u * uint32_t(Np) * DV * 2, 1024);
-  L.ap = off;
-  off = align_up(off + uint32_t(Np) * (Np + 1) / 2 * 8, 1024);
-  const uint32_t u_bytes = uint32_t(Np) * DV * 4;
-  L.u_in_x = u_bytes <= uint32_t(DK / 64) * kRegionBytes;
-  L.u = L.u_in_x ? L.x : off;
-  if (!L.u_in_x) off += u_bytes;
+  off = align_up(off + uint32_t(Np) * DV * 2, 1024);
+  L.aop = off;
+  L.ca = off;
+  L.cp = off + ncoef;
+  L.ct = off + 2 * ncoef;
+  off += 2 * kRegionBytes;
+  L.bop = off;
+  off += 2u * 2u * uint32_t(Np) * 128u;
   L.total = off;
   return L;
 }
@@ -98,15 +111,18 @@ struct TreeStage {
   float beta[kMaxNodes];
   float g[kMaxNodes];
   int par[kMaxNodes];
-  int off[kMaxNodes + 1];             // packed ancestor-coefficient offsets
+  int off[kMaxNodes + 1];             // packed per-path offsets: row t at off[t], depth(t)+1 entries
+  uint8_t dep[kMaxNodes];
+  uint8_t pnode[kMaxNodes * (kMaxNodes + 1) / 2];  // pnode[off[t] + k] = t's ancestor at depth k
+  int maxd;
   int bad;
 };
 
 struct TcShared {
   TreeStage tree[2];
   uint64_t slot_full[kMaxRing], slot_split[kMaxRing], slot_empty[kMaxRing];
-  uint64_t node_full[2], node_empty[2], gram_full[2], proj_full[2], tmem_empty[2];
-  uint64_t tree_full[2], tree_empty[2], drain;
+  uint64_t node_full[2], v_empty, gram_full[2], proj_full[2], tmem_empty[2], uo_full;
+  uint64_t tree_full[2], tree_empty[2], drain, drain_epi;
   uint32_t tmem_base;
   int abort_flag;
   int split_ok, epi_ok[3];
@@ -152,7 +168,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(DV == 64 || DV == 128, "tensor-core verify needs d_v in {64, 128}");
   constexpr int NCHUNK = DK / kChunkRows;              // ring slots per pair
   constexpr uint32_t kChunkBytes = kChunkRows * DV * 4;  // fp32 bytes of one chunk
-  constexpr uint32_t kXBytes = NCHUNK * kRegionBytes;  // one node stage of the X operand
 
   __shared__ TcShared sh;
   extern __shared__ uint8_t tc_dyn_raw[];
@@ -171,14 +186,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&sh.node_full[b], 1);
-      ptx::mbar_init(&sh.node_empty[b], kEpiThreads / 32);
       ptx::mbar_init(&sh.gram_full[b], 1);
       ptx::mbar_init(&sh.proj_full[b], 1);
       ptx::mbar_init(&sh.tmem_empty[b], kEpiThreads / 32);
       ptx::mbar_init(&sh.tree_full[b], 32);
       ptx::mbar_init(&sh.tree_empty[b], kEpiThreads / 32);
     }
+    ptx::mbar_init(&sh.v_empty, kEpiThreads / 32);
+    ptx::mbar_init(&sh.uo_full, 1);
     ptx::mbar_init(&sh.drain, 1);
+    ptx::mbar_init(&sh.drain_epi, 1);
     sh.abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -193,7 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // bookkeeping for the clean-up waits
   uint32_t issued = 0;   // state producer: chunks issued; node producer: stages issued
-  bool mma_any = false;
+  bool mma_any = false;  // the MMA warp (projections, Gram) or epilogue thread 0 (solve/output) issued MMAs
 
   if (warp == kWarpState) {
     // ------------------------------------------------------------ state producer
@@ -223,20 +240,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_v);
       const uint32_t node_bytes = uint32_t(2 * DK + DV) * Np * 2;
+      uint8_t *X = base + lay.x;
       uint32_t i = 0;
       for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
         int t0, n;
         if (!tc_pair_nodes(a, p, t0, n)) continue;
         const int h = p % a.H, b = int(i & 1u);
-        if (!tc_wait(&sh.node_empty[b], ((i >> 1) & 1u) ^ 1u, sh, a.status)) break;
-        uint8_t *X = base + lay.x + b * kXBytes;
+        // the v buffer is free once the epilogue of pair i-1 has formed its R, the X buffer once
+        // the MMAs of pair i-1 are done (neither barrier can complete again before this copy is
+        // issued, so the parity cannot have moved on)
+        if (i > 0 && !tc_wait(&sh.v_empty, (i - 1) & 1u, sh, a.status)) break;
+        if (i > 0 && !tc_wait(&sh.proj_full[(i - 1) & 1u], ((i - 1) >> 1) & 1u, sh, a.status)) break;
         ptx::mbar_arrive_expect_tx(&sh.node_full[b], node_bytes);
 #pragma unroll
         for (int c = 0; c < NCHUNK; ++c) {
           ptx::tma_load_3d(X + c * kRegionBytes, &tm_k, &sh.node_full[b], c * 64, h, t0);
           ptx::tma_load_3d(X + c * kRegionBytes + Np * 128, &tm_q, &sh.node_full[b], c * 64, h, t0);
         }
-        ptx::tma_load_3d(base + lay.v + b * (Np * DV * 2), &tm_v, &sh.node_full[b], 0, h, t0);
+        ptx::tma_load_3d(base + lay.v, &tm_v, &sh.node_full[b], 0, h, t0);
         issued = ++i;
       }
     }
@@ -254,7 +275,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!tc_wait(&sh.tmem_empty[b], ph ^ 1u, sh, a.status)) break;
         if (!tc_wait(&sh.node_full[b], ph, sh, a.status)) break;
         ptx::tc_fence_after_sync();
-        const uint32_t x0 = ptx::smem_u32(base + lay.x + b * kXBytes);
+        const uint32_t x0 = ptx::smem_u32(base + lay.x);
         const uint32_t d1 = tmem + uint32_t(b) * kTmemBuf, d2 = d1 + kGramCol;
         // Gram: A = all 128 rows of X, B = the key rows
 #pragma unroll
@@ -337,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         // exclusive prefix sum of the ancestor counts over t = 0..n-1
-        int run = 0;
+        int run = 0, offs[2] = {0, 0};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           int x = cnt[e];
@@ -347,9 +368,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane >= o) x += y;
           }
           const int t = lane + 32 * e;
-          if (t < n) ts.off[t] = run + x - cnt[e];
+          offs[e] = run + x - cnt[e];
+          if (t < n) ts.off[t] = offs[e];
           run += __shfl_sync(0xffffffffu, x, 31);
         }
+        // depth, root-to-node path table and depth levels
+        int dmax = 0;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = lane + 32 * e;
+          if (t < n) {
+            const int d = cnt[e] - 1;
+            ts.dep[t] = uint8_t(d);
+            dmax = max(dmax, d);
+            int x = t;
+            for (int k = d; k >= 0; --k) {
+              ts.pnode[offs[e] + k] = uint8_t(x);
+              x = ts.par[x];
+            }
+          }
+        }
+        dmax = __reduce_max_sync(0xffffffffu, dmax);
+        if (lane == 0) ts.maxd = dmax;
       } else if (lane == 0 && h == 0) {
         report(a.status, GDN_STATUS_BAD_TREE);
       }
@@ -361,19 +401,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= kWarpEpi && warp < kWarpEpi + kEpiThreads / 32) {
     // ------------------------------------------------------------ epilogue
     const int etid = tid - kWarpEpi * 32;
-    const int q4 = warp & 3;                // TMEM lane quarter this warp may access
-    const int row = q4 * 32 + lane;         // TMEM lane: Gram row m, or state column v
+    const int q4 = warp & 3;                     // TMEM lane quarter this warp may access
+    const int half = (warp - kWarpEpi) >> 2;     // two warps share each quarter
+    const int row = q4 * 32 + lane;              // TMEM lane: Gram row m, or state column v
     const uint32_t lane_addr = uint32_t(q4 * 32) << 16;
-    float2 *ap = reinterpret_cast<float2 *>(base + lay.ap);
+    float *cA = reinterpret_cast<float *>(base + lay.ca);
+    float *cP = reinterpret_cast<float *>(base + lay.cp);
+    float *cT = reinterpret_cast<float *>(base + lay.ct);
+    uint8_t *aop = base + lay.aop;
+    uint8_t *bop = base + lay.bop;
+    const uint32_t bop_lo = uint32_t(2 * Np * 128);
+    const uint32_t id_uo = ptx::idesc_bf16_f32(128, 2 * Np);
     uint32_t i = 0;
     for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
       int t0, n;
       if (!tc_pair_nodes(a, p, t0, n)) continue;
       const int h = p % a.H, b = int(i & 1u);
       const uint32_t ph = (i >> 1) & 1u;
-      // tree ready (the barrier also ends every epilogue thread's use of the previous pair)
-      // (each wait's verdict has its own flag, so no flag is rewritten before every thread
-      // has passed a later barrier)
+      // tree ready (the barrier also ends every epilogue thread's use of the previous pair).
+      // Each wait's verdict has its own flag, so no flag is rewritten before every thread has
+      // passed a later barrier.
       if (etid == 0) sh.epi_ok[0] = tc_wait(&sh.tree_full[b], ph, sh, a.status);
       named_sync(kBarEpi, kEpiThreads);
       if (!sh.epi_ok[0]) break;
@@ -386,7 +433,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::mbar_try_wait(&sh.gram_full[b], ph);
       ptx::tc_fence_after_sync();
       const uint32_t d1 = tmem + uint32_t(b) * kTmemBuf + lane_addr, d2 = d1 + kGramCol;
-      // masked, gated ancestor coefficients: packed {A, P} per (t, ancestor-or-self j)
+
+      // (1) masked, gated path coefficients from the Gram rows: entry (t, depth of j). All
+      // loads of the chunk happen before any store, so the stores cannot serialise them.
       if (live && q4 * 32 < 2 * Np) {
         const bool krow = row < n;
         const bool qrow = row >= Np && row - Np < n;
@@ -395,83 +444,171 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float Gt = (krow || qrow) ? ts.G[t] : 0.f;
         const float bt = krow ? ts.beta[t] : 0.f;
         const int off = (krow || qrow) ? ts.off[t] : 0;
-        for (int c0 = 0; c0 < Np; c0 += 16) {
-          float vals[16];
+        for (int c0 = 16 * half; c0 < Np; c0 += 32) {
+          float vals[16], w[16];
           ptx::tmem_ld_32x32b_x16(d2 + uint32_t(c0), vals);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) w[jj] = __expf(Gt - ts.G[c0 + jj]);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int j = c0 + jj;
-            if (j < 64 && ((anc >> j) & 1ull)) {
-              const int idx = __popcll(anc & ((1ull << j) - 1ull));
-              const float w = expf(Gt - ts.G[j]);
-              if (krow && j < t) ap[off + idx].x = bt * w * vals[jj];
-              if (qrow) ap[off + idx].y = w * vals[jj];
-            }
+            const int idx = __popcll(anc & ((1ull << j) - 1ull));
+            if (((anc >> j) & 1ull) && krow) cA[off + idx] = j < t ? bt * w[jj] * vals[jj] : 0.f;
+            if (((anc >> j) & 1ull) && qrow) cP[off + idx] = w[jj] * vals[jj];
           }
         }
       }
-      named_sync(kBarEpi, kEpiThreads);  // coefficients ready
+      ptx::tc_fence_before_sync();  // D2 is overwritten by the solve/output MMA below
+      named_sync(kBarEpi, kEpiThreads);
+
+      // (2) row t of T by a backward sweep in registers, reading only A rows along t's path:
+      //     T[t][p_d] = 1,  T[t][p_k] = -sum_{m=k+1..d} T[t][p_m] A[p_m][p_k]
+      // Meanwhile the other threads clear the [T ; W] operand.
+      if (live && etid < n) {
+        const int t = etid, d = ts.dep[t], off = ts.off[t];
+        if (d < 8) {
+          int po[8];
+          float x[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            po[m] = m <= d ? ts.off[ts.pnode[off + m]] : 0;
+            x[m] = m == d ? 1.f : 0.f;
+          }
+#pragma unroll
+          for (int k = 6; k >= 0; --k) {
+            if (k < d) {
+              float sum = 0.f;
+#pragma unroll
+              for (int m = k + 1; m < 8; ++m)
+                if (m <= d) sum = fmaf(x[m], cA[po[m] + k], sum);
+              x[k] = -sum;
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < 8; ++m)
+            if (m <= d) cT[off + m] = x[m];
+        } else {  // paths deeper than eight levels: the same sweep through shared memory
+          cT[off + d] = 1.f;
+          for (int k = d - 1; k >= 0; --k) {
+            float sum = 0.f;
+            for (int m = k + 1; m <= d; ++m) sum = fmaf(cT[off + m], cA[ts.off[ts.pnode[off + m]] + k], sum);
+            cT[off + k] = -sum;
+          }
+        }
+      }
+      for (int z = etid; z < int(bop_lo) / 8; z += kEpiThreads)  // hi and lo halves: 2 * bop_lo bytes
+        reinterpret_cast<uint4 *>(bop)[z] = make_uint4(0u, 0u, 0u, 0u);
+      named_sync(kBarEpi, kEpiThreads);
+
+      // (3) row t of W = P T: W[t][p_k] = sum_{m=k..d} P[t][p_m] T[p_m][p_k]; T and W go into the
+      // dense [T ; W] operand (row t and Np + t, column p_k) as bf16 hi + lo
+      if (live && etid < n) {
+        const int t = etid, d = ts.dep[t], off = ts.off[t];
+        for (int k = 0; k <= d; ++k) {
+          float sum = 0.f;
+          for (int m = k; m <= d; ++m) sum = fmaf(cP[off + m], cT[ts.off[ts.pnode[off + m]] + k], sum);
+          const int j = ts.pnode[off + k];
+          const float tv = cT[off + k];
+          const __nv_bfloat16 th = __float2bfloat16_rn(tv), tl = __float2bfloat16_rn(tv - __bfloat162float(th));
+          const __nv_bfloat16 wh = __float2bfloat16_rn(sum), wl = __float2bfloat16_rn(sum - __bfloat162float(wh));
+          const int rt = t, rw = Np + t;
+          const uint32_t ot = uint32_t(rt * 128 + ((((j * 2) >> 4) ^ (rt & 7)) << 4) + ((j * 2) & 15));
+          const uint32_t ow = uint32_t(rw * 128 + ((((j * 2) >> 4) ^ (rw & 7)) << 4) + ((j * 2) & 15));
+          *reinterpret_cast<__nv_bfloat16 *>(bop + ot) = th;
+          *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ot) = tl;
+          *reinterpret_cast<__nv_bfloat16 *>(bop + ow) = wh;
+          *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ow) = wl;
+        }
+      }
+
+      // (4) projections ready: R = b (v - gamma KS) -> the R^T operand (row v, column t), as
+      // bf16 hi + lo; columns t >= n are zero. The packed coefficients in these bytes are dead.
       if (etid == 0) sh.epi_ok[2] = tc_wait(&sh.proj_full[b], ph, sh, a.status);
       named_sync(kBarEpi, kEpiThreads);
       if (!sh.epi_ok[2]) break;
       ptx::mbar_try_wait(&sh.proj_full[b], ph);
       ptx::tc_fence_after_sync();
-      if (live && q4 * 32 < DV) {
-        const int v = row;
-        float *Ub = reinterpret_cast<float *>(base + lay.u + (lay.u_in_x ? b * kXBytes : 0u));
-        const uint16_t *Vs = reinterpret_cast<const uint16_t *>(base + lay.v + b * (Np * DV * 2));
-        // R = b (v - gamma KS)
-        for (int c0 = 0; c0 < n; c0 += 16) {
+      const int v = row;
+      const bool col = live && q4 * 32 < DV;
+      if (col) {
+        const uint16_t *Vs = reinterpret_cast<const uint16_t *>(base + lay.v);
+        for (int c0 = 16 * half; c0 < Np; c0 += 32) {
           float ks[16];
           ptx::tmem_ld_32x32b_x16(d1 + uint32_t(c0), ks);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int t = c0 + jj;
-            if (t < n) Ub[t * DV + v] = ts.beta[t] * (bf16_to_f32(Vs[t * DV + v]) - ts.gam[t] * ks[jj]);
+          for (int g8 = 0; g8 < 2; ++g8) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float r2[2];
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const int jj = g8 * 8 + 2 * e + z, t = c0 + jj;
+                r2[z] = t < n ? ts.beta[t] * (bf16_to_f32(Vs[t * DV + v]) - ts.gam[t] * ks[jj]) : 0.f;
+              }
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(r2[0], r2[1]);
+              const float2 hf = __bfloat1622float2(h2);
+              const __nv_bfloat162 l2 = __floats2bfloat162_rn(r2[0] - hf.x, r2[1] - hf.y);
+              hi[e] = *reinterpret_cast<const uint32_t *>(&h2);
+              lo[e] = *reinterpret_cast<const uint32_t *>(&l2);
+            }
+            const int kc = (c0 >> 3) + g8;  // 16-byte chunk along K (8 nodes)
+            const uint32_t off = uint32_t(v * 128 + ((kc ^ (v & 7)) << 4));
+            *reinterpret_cast<uint4 *>(aop + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(aop + kRegionBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
-        // forward substitution over the ancestors (parent-before-child order)
-        for (int t = 0; t < n; ++t) {
-          float uu = Ub[t * DV + v];
-          unsigned long long m = ts.anc[t] & ~(1ull << t);
-          const float2 *c = ap + ts.off[t];
-          while (m) {
-            const int j = __ffsll(m) - 1;
-            m &= m - 1;
-            uu = fmaf(-(c++)->x, Ub[j * DV + v], uu);
-          }
-          Ub[t * DV + v] = uu;
+      }
+      ptx::fence_proxy_async_smem();  // R^T and [T ; W] feed the MMA (async proxy)
+      named_sync(kBarEpi, kEpiThreads);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.v_empty);
+
+      // (5) D3 = R^T [T ; W]^T: three bf16 products (hi hi, hi lo, lo hi), fp32 accumulate
+      if (etid == 0) {
+        ptx::tc_fence_after_sync();
+        const uint32_t a0 = ptx::smem_u32(aop), b0 = ptx::smem_u32(bop);
+        const uint32_t d3 = tmem + uint32_t(b) * kTmemBuf + kGramCol;
+        for (int ks = 0; ks < Np / 16; ++ks) {
+          const uint64_t ah = ptx::desc_kmajor_sw128(a0 + ks * 32), al = ptx::desc_kmajor_sw128(a0 + kRegionBytes + ks * 32);
+          const uint64_t bh = ptx::desc_kmajor_sw128(b0 + ks * 32), bl = ptx::desc_kmajor_sw128(b0 + bop_lo + ks * 32);
+          ptx::mma_bf16_ss(d3, ah, bh, id_uo, ks > 0 ? 1u : 0u);
+          ptx::mma_bf16_ss(d3, ah, bl, id_uo, 1u);
+          ptx::mma_bf16_ss(d3, al, bh, id_uo, 1u);
         }
-        // outputs
-        for (int c0 = 0; c0 < n; c0 += 16) {
-          float qs[16];
+        ptx::mma_commit(&sh.uo_full);
+        mma_any = true;
+        sh.epi_ok[0] = tc_wait(&sh.uo_full, i & 1u, sh, a.status);
+      }
+      named_sync(kBarEpi, kEpiThreads);
+      if (!sh.epi_ok[0]) break;
+      ptx::mbar_try_wait(&sh.uo_full, i & 1u);
+      ptx::tc_fence_after_sync();
+
+      // (6) u_t = D3[:, t], o_t = gamma_t QS_t + D3[:, Np + t]
+      if (col) {
+        const uint32_t d3 = d2;
+        for (int c0 = 16 * half; c0 < n; c0 += 32) {
+          float uu[16], ww[16], qs[16];
+          ptx::tmem_ld_32x32b_x16(d3 + uint32_t(c0), uu);
+          ptx::tmem_ld_32x32b_x16(d3 + uint32_t(Np + c0), ww);
           ptx::tmem_ld_32x32b_x16(d1 + uint32_t(Np + c0), qs);
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) {
             const int t = c0 + jj;
             if (t < n) {
-              float out = ts.gam[t] * qs[jj];
-              unsigned long long m = ts.anc[t];
-              const float2 *c = ap + ts.off[t];
-              while (m) {
-                const int j = __ffsll(m) - 1;
-                m &= m - 1;
-                out = fmaf((c++)->y, Ub[j * DV + v], out);
-              }
               const size_t o_row = (size_t(t0 + t) * a.H + h) * DV + v;
-              __stcs(a.o + o_row, out);
-              __stcs(a.U + o_row, Ub[t * DV + v]);
+              __stcs(a.o + o_row, fmaf(ts.gam[t], qs[jj], ww[jj]));
+              __stcs(a.U + o_row, uu[jj]);
             }
           }
         }
       }
       if (live && etid < n) a.G[size_t(t0 + etid) * a.H + h] = ts.G[etid];
       ptx::tc_fence_before_sync();
-      ptx::fence_proxy_async_smem();  // U was written into the node stage the TMA reuses
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sh.tmem_empty[b]);
-        mbar_arrive(&sh.node_empty[b]);
         mbar_arrive(&sh.tree_empty[b]);
       }
       ++i;
@@ -548,6 +685,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == kWarpMma && lane == 0 && mma_any) {
     ptx::mma_commit(&sh.drain);
     ptx::mbar_wait(&sh.drain, 0, kWaitLimitNs);
+  }
+  if (tid == kWarpEpi * 32 && mma_any) {
+    ptx::mma_commit(&sh.drain_epi);
+    ptx::mbar_wait(&sh.drain_epi, 0, kWaitLimitNs);
   }
   ptx::tc_fence_before_sync();
   __syncthreads();
