@@ -114,6 +114,9 @@ struct TreeStage {
   int off[kMaxNodes + 1];             // packed per-path offsets: row t at off[t], depth(t)+1 entries
   uint8_t dep[kMaxNodes];
   uint8_t pnode[kMaxNodes * (kMaxNodes + 1) / 2];  // pnode[off[t] + k] = t's ancestor at depth k
+  uint8_t tnode[kMaxNodes * (kMaxNodes + 1) / 2];  // tnode[off[t] + k] = t
+  int16_t poff[kMaxNodes * (kMaxNodes + 1) / 2];   // poff[e] = off[pnode[e]]
+  int nent;                                        // path entries of the pair
   int maxd;
   int bad;
 };
@@ -121,7 +124,7 @@ struct TreeStage {
 struct TcShared {
   TreeStage tree[2];
   uint64_t slot_full[kMaxRing], slot_split[kMaxRing], slot_empty[kMaxRing];
-  uint64_t node_full[2], v_empty, gram_full[2], proj_full[2], tmem_empty[2], uo_full;
+  uint64_t node_full[2], v_full, v_empty, gram_full[2], proj_full[2], tmem_empty[2], uo_full;
   uint64_t tree_full[2], tree_empty[2], drain, drain_epi;
   uint32_t tmem_base;
   int abort_flag;
@@ -192,6 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::mbar_init(&sh.tree_full[b], 32);
       ptx::mbar_init(&sh.tree_empty[b], kEpiThreads / 32);
     }
+    ptx::mbar_init(&sh.v_full, 1);
     ptx::mbar_init(&sh.v_empty, kEpiThreads / 32);
     ptx::mbar_init(&sh.uo_full, 1);
     ptx::mbar_init(&sh.drain, 1);
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // bookkeeping for the clean-up waits
   uint32_t issued = 0;   // state producer: chunks issued; node producer: stages issued
+  uint32_t v_issued = 0; // node producer: v copies issued
   bool mma_any = false;  // the MMA warp (projections, Gram) or epilogue thread 0 (solve/output) issued MMAs
 
   if (warp == kWarpState) {
@@ -239,26 +244,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_v);
-      const uint32_t node_bytes = uint32_t(2 * DK + DV) * Np * 2;
+      const uint32_t x_bytes = uint32_t(2 * DK) * Np * 2, v_bytes = uint32_t(DV) * Np * 2;
       uint8_t *X = base + lay.x;
       uint32_t i = 0;
       for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
         int t0, n;
         if (!tc_pair_nodes(a, p, t0, n)) continue;
         const int h = p % a.H, b = int(i & 1u);
-        // the v buffer is free once the epilogue of pair i-1 has formed its R, the X buffer once
-        // the MMAs of pair i-1 are done (neither barrier can complete again before this copy is
-        // issued, so the parity cannot have moved on)
-        if (i > 0 && !tc_wait(&sh.v_empty, (i - 1) & 1u, sh, a.status)) break;
+        // the X buffer is free once the MMAs of pair i-1 are done, the v buffer once the
+        // epilogue of pair i-1 has formed its R (neither barrier can complete again before
+        // this copy is issued, so the parity cannot have moved on); X goes first so the MMAs
+        // never wait on v
         if (i > 0 && !tc_wait(&sh.proj_full[(i - 1) & 1u], ((i - 1) >> 1) & 1u, sh, a.status)) break;
-        ptx::mbar_arrive_expect_tx(&sh.node_full[b], node_bytes);
+        ptx::mbar_arrive_expect_tx(&sh.node_full[b], x_bytes);
 #pragma unroll
         for (int c = 0; c < NCHUNK; ++c) {
           ptx::tma_load_3d(X + c * kRegionBytes, &tm_k, &sh.node_full[b], c * 64, h, t0);
           ptx::tma_load_3d(X + c * kRegionBytes + Np * 128, &tm_q, &sh.node_full[b], c * 64, h, t0);
         }
-        ptx::tma_load_3d(base + lay.v, &tm_v, &sh.node_full[b], 0, h, t0);
         issued = ++i;
+        if (i > 1 && !tc_wait(&sh.v_empty, (i - 2) & 1u, sh, a.status)) break;
+        ptx::mbar_arrive_expect_tx(&sh.v_full, v_bytes);
+        ptx::tma_load_3d(base + lay.v, &tm_v, &sh.v_full, 0, h, t0);
+        v_issued = i;
       }
     }
   } else if (warp == kWarpMma) {
@@ -384,12 +392,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int x = t;
             for (int k = d; k >= 0; --k) {
               ts.pnode[offs[e] + k] = uint8_t(x);
+              ts.tnode[offs[e] + k] = uint8_t(t);
               x = ts.par[x];
             }
           }
         }
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = lane + 32 * e;
+          if (t < n)
+            for (int k = 0; k < cnt[e]; ++k) ts.poff[offs[e] + k] = int16_t(ts.off[ts.pnode[offs[e] + k]]);
+        }
         dmax = __reduce_max_sync(0xffffffffu, dmax);
-        if (lane == 0) ts.maxd = dmax;
+        if (lane == 0) {
+          ts.maxd = dmax;
+          ts.nent = run;
+        }
       } else if (lane == 0 && h == 0) {
         report(a.status, GDN_STATUS_BAD_TREE);
       }
@@ -434,36 +453,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::tc_fence_after_sync();
       const uint32_t d1 = tmem + uint32_t(b) * kTmemBuf + lane_addr, d2 = d1 + kGramCol;
 
-      // (1) masked, gated path coefficients from the Gram rows: entry (t, depth of j). All
-      // loads of the chunk happen before any store, so the stores cannot serialise them.
+      // (1) raw Gram rows -> the [T ; W] operand bytes, fp32 [2Np][Np] with each row's 16-byte
+      // chunks rotated by the row index (fewer bank conflicts); this region is free until (3)
+      float *gram = reinterpret_cast<float *>(bop);
+      const int nq = Np / 4;  // 16-byte chunks per Gram row
       if (live && q4 * 32 < 2 * Np) {
-        const bool krow = row < n;
-        const bool qrow = row >= Np && row - Np < n;
-        const int t = krow ? row : row - Np;
-        const unsigned long long anc = (krow || qrow) ? ts.anc[t] : 0ull;
-        const float Gt = (krow || qrow) ? ts.G[t] : 0.f;
-        const float bt = krow ? ts.beta[t] : 0.f;
-        const int off = (krow || qrow) ? ts.off[t] : 0;
         for (int c0 = 16 * half; c0 < Np; c0 += 32) {
-          float vals[16], w[16];
+          float vals[16];
           ptx::tmem_ld_32x32b_x16(d2 + uint32_t(c0), vals);
+          if (row < 2 * Np) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) w[jj] = __expf(Gt - ts.G[c0 + jj]);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = c0 + jj;
-            const int idx = __popcll(anc & ((1ull << j) - 1ull));
-            if (((anc >> j) & 1ull) && krow) cA[off + idx] = j < t ? bt * w[jj] * vals[jj] : 0.f;
-            if (((anc >> j) & 1ull) && qrow) cP[off + idx] = w[jj] * vals[jj];
+            for (int c = 0; c < 4; ++c) {
+              const int cq = (c0 / 4 + c + row) % nq;
+              *reinterpret_cast<float4 *>(gram + row * Np + cq * 4) =
+                  make_float4(vals[4 * c], vals[4 * c + 1], vals[4 * c + 2], vals[4 * c + 3]);
+            }
           }
         }
       }
       ptx::tc_fence_before_sync();  // D2 is overwritten by the solve/output MMA below
       named_sync(kBarEpi, kEpiThreads);
 
-      // (2) row t of T by a backward sweep in registers, reading only A rows along t's path:
-      //     T[t][p_d] = 1,  T[t][p_k] = -sum_{m=k+1..d} T[t][p_m] A[p_m][p_k]
-      // Meanwhile the other threads clear the [T ; W] operand.
+      // (2a) masked, gated path coefficients, one thread per path entry e = (t, depth k of j):
+      //      A = b_t exp(G_t - G_j) k_t.k_j (0 for j = t),  P = exp(G_t - G_j) q_t.k_j
+      const int nent = live ? ts.nent : 0;
+      for (int e = etid; e < nent; e += kEpiThreads) {
+        const int t = ts.tnode[e], j = ts.pnode[e];
+        const float w = __expf(ts.G[t] - ts.G[j]);
+        const int cj = ((j >> 2) + t) % nq, cjq = ((j >> 2) + Np + t) % nq;
+        const float kk = gram[t * Np + cj * 4 + (j & 3)];
+        const float qk = gram[(Np + t) * Np + cjq * 4 + (j & 3)];
+        cA[e] = j == t ? 0.f : ts.beta[t] * w * kk;
+        cP[e] = w * qk;
+      }
+      named_sync(kBarEpi, kEpiThreads);
+
+      // (2b) row t of T by a backward sweep in registers, reading only A rows along t's path:
+      //      T[t][p_d] = 1,  T[t][p_k] = -sum_{m=k+1..d} T[t][p_m] A[p_m][p_k]
+      // Meanwhile the other threads clear the [T ; W] operand (the raw Gram is consumed).
       if (live && etid < n) {
         const int t = etid, d = ts.dep[t], off = ts.off[t];
         if (d < 8) {
@@ -471,7 +498,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float x[8];
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
-            po[m] = m <= d ? ts.off[ts.pnode[off + m]] : 0;
+            po[m] = m <= d ? ts.poff[off + m] : 0;
             x[m] = m == d ? 1.f : 0.f;
           }
 #pragma unroll
@@ -491,7 +518,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cT[off + d] = 1.f;
           for (int k = d - 1; k >= 0; --k) {
             float sum = 0.f;
-            for (int m = k + 1; m <= d; ++m) sum = fmaf(cT[off + m], cA[ts.off[ts.pnode[off + m]] + k], sum);
+            for (int m = k + 1; m <= d; ++m) sum = fmaf(cT[off + m], cA[ts.poff[off + m] + k], sum);
             cT[off + k] = -sum;
           }
         }
@@ -500,33 +527,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         reinterpret_cast<uint4 *>(bop)[z] = make_uint4(0u, 0u, 0u, 0u);
       named_sync(kBarEpi, kEpiThreads);
 
-      // (3) row t of W = P T: W[t][p_k] = sum_{m=k..d} P[t][p_m] T[p_m][p_k]; T and W go into the
-      // dense [T ; W] operand (row t and Np + t, column p_k) as bf16 hi + lo
-      if (live && etid < n) {
-        const int t = etid, d = ts.dep[t], off = ts.off[t];
-        for (int k = 0; k <= d; ++k) {
-          float sum = 0.f;
-          for (int m = k; m <= d; ++m) sum = fmaf(cP[off + m], cT[ts.off[ts.pnode[off + m]] + k], sum);
-          const int j = ts.pnode[off + k];
-          const float tv = cT[off + k];
-          const __nv_bfloat16 th = __float2bfloat16_rn(tv), tl = __float2bfloat16_rn(tv - __bfloat162float(th));
-          const __nv_bfloat16 wh = __float2bfloat16_rn(sum), wl = __float2bfloat16_rn(sum - __bfloat162float(wh));
-          const int rt = t, rw = Np + t;
-          const uint32_t ot = uint32_t(rt * 128 + ((((j * 2) >> 4) ^ (rt & 7)) << 4) + ((j * 2) & 15));
-          const uint32_t ow = uint32_t(rw * 128 + ((((j * 2) >> 4) ^ (rw & 7)) << 4) + ((j * 2) & 15));
-          *reinterpret_cast<__nv_bfloat16 *>(bop + ot) = th;
-          *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ot) = tl;
-          *reinterpret_cast<__nv_bfloat16 *>(bop + ow) = wh;
-          *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ow) = wl;
-        }
+      // (3) W = P T, one thread per path entry: W[t][p_k] = sum_{m=k..d} P[t][p_m] T[p_m][p_k].
+      // T and W go into the dense [T ; W] operand (row t and Np + t, column p_k), bf16 hi + lo.
+      for (int e = etid; e < nent; e += kEpiThreads) {
+        const int t = ts.tnode[e], j = ts.pnode[e], off = ts.off[t], d = ts.dep[t], k = e - off;
+        float sum = 0.f;
+        for (int m = k; m <= d; ++m) sum = fmaf(cP[off + m], cT[ts.poff[off + m] + k], sum);
+        const float tv = cT[e];
+        const __nv_bfloat16 th = __float2bfloat16_rn(tv), tl = __float2bfloat16_rn(tv - __bfloat162float(th));
+        const __nv_bfloat16 wh = __float2bfloat16_rn(sum), wl = __float2bfloat16_rn(sum - __bfloat162float(wh));
+        const int rt = t, rw = Np + t;
+        const uint32_t ot = uint32_t(rt * 128 + ((((j * 2) >> 4) ^ (rt & 7)) << 4) + ((j * 2) & 15));
+        const uint32_t ow = uint32_t(rw * 128 + ((((j * 2) >> 4) ^ (rw & 7)) << 4) + ((j * 2) & 15));
+        *reinterpret_cast<__nv_bfloat16 *>(bop + ot) = th;
+        *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ot) = tl;
+        *reinterpret_cast<__nv_bfloat16 *>(bop + ow) = wh;
+        *reinterpret_cast<__nv_bfloat16 *>(bop + bop_lo + ow) = wl;
       }
 
       // (4) projections ready: R = b (v - gamma KS) -> the R^T operand (row v, column t), as
       // bf16 hi + lo; columns t >= n are zero. The packed coefficients in these bytes are dead.
-      if (etid == 0) sh.epi_ok[2] = tc_wait(&sh.proj_full[b], ph, sh, a.status);
+      if (etid == 0)
+        sh.epi_ok[2] = tc_wait(&sh.proj_full[b], ph, sh, a.status) && tc_wait(&sh.v_full, i & 1u, sh, a.status);
       named_sync(kBarEpi, kEpiThreads);
       if (!sh.epi_ok[2]) break;
       ptx::mbar_try_wait(&sh.proj_full[b], ph);
+      ptx::mbar_try_wait(&sh.v_full, i & 1u);
       ptx::tc_fence_after_sync();
       const int v = row;
       const bool col = live && q4 * 32 < DV;
@@ -681,6 +707,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::mbar_wait(&sh.node_full[b], (last >> 1) & 1u, kWaitLimitNs);
       }
     }
+    if (v_issued > 0) ptx::mbar_wait(&sh.v_full, (v_issued - 1) & 1u, kWaitLimitNs);
   }
   if (warp == kWarpMma && lane == 0 && mma_any) {
     ptx::mma_commit(&sh.drain);
