@@ -36,9 +36,10 @@ sys.path.insert(0, ROOT)
 METRIC = "draft-node verifications/sec (verify+commit) and achieved HBM GB/s vs B300 peak"
 UNIT = "node-verifications/s"
 KERNEL_SOURCES = {
-    "verify": ["verify_tc.cuh", "verify_simt.cuh", "common.cuh", "ptx.cuh"],
-    "commit": ["commit.cuh", "common.cuh"],
+    "verify": ["verify_stream.cuh", "verify_tc.cuh", "verify_simt.cuh", "common.cuh", "ptx.cuh"],
+    "commit": ["commit.cuh", "common.cuh", "ptx.cuh"],
 }
+NOMINAL_HBM_GBS = 8000.0  # the B300 HBM3e figure the roofline target is quoted against
 
 
 # ---------------------------------------------------------------------------
@@ -182,14 +183,22 @@ def shard_layers(rank: int, n_layers: int) -> list[int]:
 # workloads
 # ---------------------------------------------------------------------------
 
+WORKLOAD_NAMES = {
+    0: ("chain3_d32", "chain of 3 draft nodes, B=1, H=1, d_k=d_v=32"),
+    1: ("chain4", "depth-3 chain (4 nodes incl. bonus), B={B}, H=32, d_k=d_v=128, fp32 state, bf16 q/k/v"),
+    2: ("rootbranch6", "6-node root-branch tree, B={B}, H=48, d_k=d_v=128, fp32 state, bf16 q/k/v"),
+    3: ("ragged16to64", "ragged random trees of 16-64 nodes (fanout<=4, depth<=8), B={B}, H=32, d_k=d_v=128"),
+    4: ("tree32", "32-node random trees (fanout<=3, depth<=6), B={B}, H=32, d_k=d_v=128, gate a~U(0.85,1)"),
+}
+
+
 def workload_name(cfg: int, batch: int) -> str:
-    return {
-        0: "config0: chain of 3, B=1, H=1, d=32",
-        1: f"config1: depth-3 chain (4 nodes incl. bonus), B={batch}, H=32, d_k=d_v=128, fp32 state, bf16 q/k/v",
-        2: f"config2: 6-node root-branch tree, B={batch}, H=48, d=128",
-        3: f"config3: ragged random trees of 16-64 nodes, B={batch}, H=32, d=128",
-        4: f"config4: 32-node random trees, B={batch}, H=32, d=128, gate a~U(0.85,1)",
-    }[cfg]
+    return WORKLOAD_NAMES[cfg][1].format(B=batch)
+
+
+def workload_key(cfg: int, batch: int) -> str:
+    """Short label of a workload and batch, as used in profiles/traffic.txt."""
+    return f"{WORKLOAD_NAMES[cfg][0]}_B{batch}"
 
 
 def make_layers(cfg: int, batch: int, layer_ids):
@@ -347,11 +356,14 @@ def run_ours(args):
         "verify+commit": {"ms": v_ms + c_ms, "GB/s": (vb + cb) / ((v_ms + c_ms) * 1e6),
                           "frac": (vb + cb) / ((v_ms + c_ms) * 1e6) / peaks["hbm_gbs"]},
     }
+    for kd in kernels.values():
+        kd["frac_of_nominal"] = kd["GB/s"] / NOMINAL_HBM_GBS
     dom = "verify" if v_ms >= c_ms else "commit"
-    wl = f"config{args.config}"
+    wl = workload_key(args.config, tb0.B)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["GB/s"], "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": kernels[dom]["frac"], "peak_source": peaks["source"],
-                "traffic": ncu_traffic(dom, wl)}
+                "traffic": ncu_traffic(dom, wl), "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_of_nominal": kernels[dom]["GB/s"] / NOMINAL_HBM_GBS}
 
     # end to end: pinned host inputs -> device, verify + commit, outputs -> pinned host
     e2e = None

@@ -174,7 +174,9 @@ gdn_status launch_verify_stream(const VerifyArgs &a, cudaStream_t stream) {
 
 template <int DK, int DV>
 gdn_status launch_verify_stream_n(const VerifyArgs &a, cudaStream_t stream) {
-  return a.max_nodes <= 4 ? launch_verify_stream<DK, DV, 4>(a, stream) : launch_verify_stream<DK, DV, 8>(a, stream);
+  if (a.max_nodes <= 4) return launch_verify_stream<DK, DV, 4>(a, stream);
+  if (a.max_nodes <= 6) return launch_verify_stream<DK, DV, 6>(a, stream);
+  return launch_verify_stream<DK, DV, 8>(a, stream);
 }
 
 template <int DK, int DV>

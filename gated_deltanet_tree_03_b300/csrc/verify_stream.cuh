@@ -30,8 +30,12 @@ __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
   return make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
 }
 
+// Register cap per thread, sized so that 14 (four nodes), 11 (six) or 9 (eight) 64-thread CTAs
+// share an SM.
+__host__ __device__ constexpr int stream_max_regs(int nmax) { return nmax <= 4 ? 72 : nmax <= 6 ? 88 : 112; }
+
 template <int DK, int DV, int NMAX>
-__global__ void __launch_bounds__(DV / 2) verify_stream_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) verify_stream_kernel(VerifyArgs a) {
   constexpr int NT = DV / 2;    // threads
   constexpr int NW = NT / 32;   // warps
   constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
@@ -45,7 +49,8 @@ __global__ void __launch_bounds__(DV / 2) verify_stream_kernel(VerifyArgs a) {
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pair = blockIdx.x, h = pair % a.H, r = pair / a.H;
-  const float2 *st = reinterpret_cast<const float2 *>(a.ST + size_t(pair) * DK * DV) + tid;
+  const int col2 = tid;  // this thread's float2 column index within a state row
+  const float2 *st = reinterpret_cast<const float2 *>(a.ST + size_t(pair) * DK * DV) + col2;
 
   // 1) the first state rows go out before any dependent load
   float2 s[kStreamPF];
@@ -82,7 +87,7 @@ __global__ void __launch_bounds__(DV / 2) verify_stream_kernel(VerifyArgs a) {
   uint32_t vb[NMAX];
 #pragma unroll
   for (int t = 0; t < NMAX; ++t)
-    vb[t] = t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * tid) : 0u;
+    vb[t] = t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
   int bad = 0;
   if (tid < n) {
     const int p = a.parent[t0 + tid];
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(DV / 2) verify_stream_kernel(VerifyArgs a) {
           o.y = fmaf(c, u[j].y, o.y);
         }
       }
-      const size_t row = (size_t(t0 + t) * H + h) * DV2 + tid;
+      const size_t row = (size_t(t0 + t) * H + h) * DV2 + col2;
       __stcs(reinterpret_cast<float2 *>(a.o) + row, o);
       __stcs(reinterpret_cast<float2 *>(a.U) + row, u[t]);
     }

@@ -240,10 +240,10 @@ def test_bad_offsets_reported(kernel):
 
 
 @pytest.mark.parametrize("dk,dv", [(128, 128), (64, 64), (64, 128), (128, 64), (32, 128), (32, 64)])
-@pytest.mark.parametrize("nmax", [4, 8])
+@pytest.mark.parametrize("nmax", [4, 6, 8])
 def test_small_trees_streaming_kernel(dk, dv, nmax):
     """Trees of at most 8 nodes (forests, random topological orders, empty requests) take the
-    register-resident streaming kernel; both of its node capacities (4 and 8)."""
+    register-resident streaming kernel; each of its node capacities (4, 6 and 8)."""
     rng = np.random.default_rng(1000 + dk + dv + nmax)
     parents, paths = [], []
     for r in range(13):
