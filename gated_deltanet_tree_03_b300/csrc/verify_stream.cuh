@@ -5,7 +5,7 @@
 // One CTA per (request, head), DV/2 threads; thread i owns state columns 2i and 2i+1. The CTA
 // issues its first state rows before anything else, then stages the node block (keys and
 // queries widened to fp32) in shared memory and analyses the tree while those loads are in
-// flight. The fp32 state then streams from HBM exactly once, kStreamPF rows ahead of use, and
+// flight. The fp32 state then streams from HBM exactly once, 16 rows ahead of use, and
 // every row updates the thread's 2 x 2*NMAX projection accumulators
 //     KS_t = S_0 k_t,   QS_t = S_0 q_t            (fp32 FMA, fp32 accumulate)
 // Per node (registers, loops fully unrolled over the NMAX slots, ancestor tests uniform across
@@ -23,7 +23,6 @@
 
 namespace gdn {
 
-constexpr int kStreamPF = 16;       // state rows in flight per thread
 constexpr int kStreamMaxNodes = 8;  // largest tree the streaming kernel takes
 
 __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
@@ -34,12 +33,16 @@ __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
 // share an SM.
 __host__ __device__ constexpr int stream_max_regs(int nmax) { return nmax <= 4 ? 72 : nmax <= 6 ? 88 : 112; }
 
+// State rows each thread keeps in flight (more rows cost resident CTAs; 16 measured best).
+__host__ __device__ constexpr int stream_prefetch_rows(int) { return 16; }
+
 template <int DK, int DV, int NMAX>
 __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) verify_stream_kernel(VerifyArgs a) {
   constexpr int NT = DV / 2;    // threads
   constexpr int NW = NT / 32;   // warps
   constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
   constexpr int DV2 = DV / 2;   // float2 per state row
+  constexpr int kStreamPF = stream_prefetch_rows(NMAX);
   static_assert(NMAX <= 8 && DK % kStreamPF == 0 && NT % 32 == 0, "shape");
   __shared__ __align__(16) float Xs[NX][DK];
   __shared__ float Ac[NMAX][NMAX], Pc[NMAX][NMAX];
