@@ -374,13 +374,36 @@ def run_ours(args):
         h2d = sum(host_in[0][k].numel() * host_in[0][k].element_size() for k in keys)
         d2h = host_o[0].numel() * host_o[0].element_size()
         Ke = max(1, min(K, args.e2e_steps))
+        # three streams: copies in, the hot path, copies out; step i's inputs arrive while step i-1
+        # runs and step i-1's outputs leave while step i runs. Each layer's buffers are reused only
+        # after the step that last used them has finished with them.
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        nl = len(layers)
+        comp_done = [None] * nl  # last hot-path event per layer (its inputs may be overwritten after)
+        out_done = [None] * nl   # last copy-out event per layer (its o may be overwritten after)
 
         def e2e_step(i):
-            j = i % len(layers)
-            for k in keys:
-                dev_in[j][k].copy_(host_in[j][k], non_blocking=True)
+            j = i % nl
+            with torch.cuda.stream(s_in):
+                if comp_done[j] is not None:
+                    s_in.wait_event(comp_done[j])
+                for k in keys:
+                    dev_in[j][k].copy_(host_in[j][k], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            if out_done[j] is not None:
+                stream.wait_event(out_done[j])
             commit(*step(i))
-            host_o[j].copy_(dev_out[j]["o"], non_blocking=True)
+            ev_c = torch.cuda.Event()
+            ev_c.record(stream)
+            comp_done[j] = ev_c
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_c)
+                host_o[j].copy_(dev_out[j]["o"], non_blocking=True)
+                ev_o = torch.cuda.Event()
+                ev_o.record(s_out)
+            out_done[j] = ev_o
 
         for i in range(args.warmup):
             e2e_step(i)
@@ -388,15 +411,21 @@ def run_ours(args):
         if dist is not None:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(s_in)
+        stream.wait_event(e0)
+        s_out.wait_event(e0)
         for i in range(Ke):
             e2e_step(i)
-        e1.record(stream)
+        for ev in out_done:
+            if ev is not None:
+                s_in.wait_event(ev)
+        e1.record(s_in)
         torch.cuda.synchronize()
         ems = max_over_ranks(dist, e0.elapsed_time(e1), dev)
         e2e = {"value": nodes_per_step * world * Ke / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": Ke,
-               "note": "state resident in HBM across steps; per-step node block, tree and paths copied in, o copied out"}
+               "note": "state resident in HBM across steps; every step copies its node block, tree and paths in "
+                       "from pinned host memory and its o out, on copy streams overlapping the neighbouring steps"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
