@@ -17,6 +17,7 @@ from . import _build
 
 GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
 STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8, 16
+STATUS_PATH_TRUNCATED = 32
 MAX_NODES = 64
 
 HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
@@ -44,6 +45,7 @@ _SIGS = {
     "gdn_tree_commit": [_P] * 8 + [_I] * 6 + [_P, _P],
     "gdn_tree_verify_storeall": [_P] * 8 + [_I] * 6 + [_P] * 5 + [_P],
     "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 6 + [_P, _P],
+    "gdn_tree_accept_greedy": [_P] * 4 + [_I] * 4 + [_P] * 3 + [_P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -138,3 +140,10 @@ def gdn_tree_commit_storeall(ST, snapshots, parent, cu_nodes, path, path_len, B,
     _check(_lib.gdn_tree_commit_storeall(_ptr(ST), _ptr(snapshots), _ptr(parent), _ptr(cu_nodes),
                                          _ptr(path), _ptr(path_len), B, H, T, d_k, d_v, max_path,
                                          _ptr(status), _stream(stream)), "gdn_tree_commit_storeall")
+
+
+def gdn_tree_accept_greedy(draft_tok, target_tok, parent, cu_nodes, B, T, max_nodes, max_path, path, path_len,
+                           status=None, stream=None):
+    _check(_lib.gdn_tree_accept_greedy(_ptr(draft_tok), _ptr(target_tok), _ptr(parent), _ptr(cu_nodes), B, T,
+                                       max_nodes, max_path, _ptr(path), _ptr(path_len), _ptr(status),
+                                       _stream(stream)), "gdn_tree_accept_greedy")

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "gdn_tree.h"
+#include "accept.cuh"
 #include "common.cuh"
 #include "commit.cuh"
 #include "storeall.cuh"
@@ -285,6 +286,26 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
     case 128064: return launch_commit<128, 64>(a, s);
     default: return launch_commit<128, 128>(a, s);
   }
+}
+
+gdn_status gdn_tree_accept_greedy(const int32_t *draft_tok, const int32_t *target_tok,
+                                  const int32_t *parent, const int32_t *cu_nodes, int32_t B,
+                                  int32_t T, int32_t max_nodes, int32_t max_path, int32_t *path,
+                                  int32_t *path_len, int32_t *status, gdn_stream_t stream) {
+  if (B < 0 || T < 0 || max_nodes < 0 || max_path < 0) return GDN_EINVAL;
+  if (max_nodes > kMaxNodes || max_path > kMaxNodes) return GDN_ETOOBIG;
+  if (B == 0) return GDN_OK;
+  if (!cu_nodes || !path_len || (max_path > 0 && !path)) return GDN_EINVAL;
+  if (T > 0 && (!draft_tok || !target_tok || !parent)) return GDN_EINVAL;
+  const void *ptrs[] = {draft_tok, target_tok, parent, cu_nodes, path, path_len, status};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_EALIGN;
+  gdn_status st;
+  if ((st = check_device()) != GDN_OK) return st;
+  AcceptArgs a{draft_tok, target_tok, parent, cu_nodes, B, T, max_nodes, max_path, path, path_len, status};
+  const unsigned blocks = unsigned((B + kAcceptWarps - 1) / kAcceptWarps);
+  accept_greedy_kernel<<<blocks, kAcceptWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
 }
 
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,

@@ -362,3 +362,27 @@ def make_random_batch(seed: int, B: int, H: int, d: int, n_range=(1, 16), fanout
         full = root_path(p, lv[int(rng.integers(len(lv)))])
         paths.append(full[:int(rng.integers(0, len(full) + 1))])
     return build_batch(rng, parents, paths, H=H, dk=d, dv=d, gate=gate, name=f"random_seed{seed}")
+
+
+def draw_tokens(rng: np.random.Generator, parent: np.ndarray, cu_nodes: np.ndarray, vocab: int = 50,
+                p_match: float = 0.7):
+    """Synthetic draft / target tokens for greedy acceptance tests.
+
+    draft_tok[t] is uniform over the vocabulary. target_tok[x] (the target's greedy token after
+    node x) equals the draft token of one of x's children, chosen uniformly, with probability
+    p_match, and is uniform otherwise (a leaf always gets a uniform token).
+    """
+    T = int(cu_nodes[-1])
+    draft = rng.integers(0, vocab, size=T).astype(np.int32)
+    target = rng.integers(0, vocab, size=T).astype(np.int32)
+    for r in range(len(cu_nodes) - 1):
+        t0, t1 = int(cu_nodes[r]), int(cu_nodes[r + 1])
+        children = [[] for _ in range(t1 - t0)]
+        for t in range(t0, t1):
+            p = int(parent[t])
+            if p >= 0:
+                children[p].append(t - t0)
+        for x in range(t1 - t0):
+            if children[x] and rng.random() < p_match:
+                target[t0 + x] = draft[t0 + children[x][int(rng.integers(len(children[x])))]]
+    return draft, target

@@ -74,6 +74,7 @@ typedef enum gdn_status {
 #define GDN_STATUS_TOO_MANY_NODES 4u /* a request has more than max_nodes nodes              */
 #define GDN_STATUS_TIMEOUT 8u        /* a bounded wait on an asynchronous copy gave up       */
 #define GDN_STATUS_BAD_OFFSETS 16u   /* cu_nodes not non-decreasing inside [0, T]            */
+#define GDN_STATUS_PATH_TRUNCATED 32u /* an accepted path was longer than max_path            */
 
 /*
  * gdn_tree_verify - outputs and pseudo-values of every draft node (tree-structured WY form).
@@ -154,6 +155,32 @@ gdn_status gdn_tree_commit_storeall(float *ST, const float *snapshots, const int
                                     const int32_t *path_len, int32_t B, int32_t H, int32_t T,
                                     int32_t d_k, int32_t d_v, int32_t max_path,
                                     int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_accept_greedy - the accepted path of every request, found on the device so that
+ * verify -> accept -> commit runs without a host round trip (GDN Tree-Scan abstract: device-side
+ * commitment of the accepted chain; TreeWY page, method section: candidate outputs decide
+ * acceptance, after which only the accepted path's state is rebuilt).
+ *
+ * Greedy matching: the path starts at node 0 (the first root: the token the target already
+ * produced, always kept) and, at the current node x, moves to the lowest-indexed child c with
+ * draft_tok[c] == target_tok[x]; it stops when no child matches.
+ *
+ *   draft_tok   [T] int32   in   token proposed at each node
+ *   target_tok  [T] int32   in   the target's greedy (argmax) next token after each node
+ *   parent, cu_nodes        in   the tree, as for gdn_tree_verify
+ *   B, T, max_nodes         in   sizes, as for gdn_tree_verify
+ *   max_path                in   row length of path (>= 1 to accept anything)
+ *   path     [B][max_path]  out  request-local node ids, root first; unused slots -1
+ *   path_len [B]            out  0 for an empty, rejected or malformed request
+ *   status                  out  optional: BAD_TREE, BAD_OFFSETS, TOO_MANY_NODES, PATH_TRUNCATED
+ *                                (the path is cut at max_path nodes)
+ * The outputs feed gdn_tree_commit directly.
+ */
+gdn_status gdn_tree_accept_greedy(const int32_t *draft_tok, const int32_t *target_tok,
+                                  const int32_t *parent, const int32_t *cu_nodes, int32_t B,
+                                  int32_t T, int32_t max_nodes, int32_t max_path, int32_t *path,
+                                  int32_t *path_len, int32_t *status, gdn_stream_t stream);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);

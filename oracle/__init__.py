@@ -9,7 +9,9 @@ Two implementations of the same definition:
     ``verify`` / ``commit`` (optionally on a sampled list of pairs).
   * ``replay.py``    - a NumPy twin for small cases.
 
-Parity pins live in ``tests/test_oracle_pins.py``: a hand-worked d=2 example
+Greedy acceptance (``accept_greedy``) is plain Python loops over the tree.
+
+Parity pins live in ``tests/test_oracle_pins.py`` and ``tests/test_accept_pins.py``: a hand-worked d=2 example
 (``tests/golden/``), closed forms of the rule (no-write, pure decay, delta-rule erasure,
 orthonormal keys), linearity, chain = sequential decode, branch extraction, topological
 relabelling, and brute-force store-all stepping on tiny inputs.
@@ -174,6 +176,11 @@ def commit(ST0, k, v, beta, g, parent, cu_nodes, path, path_len, pairs=None, n_t
     if pairs is None:
         return out.reshape(B, H, dk, dv)
     return out
+
+
+def accept_greedy(draft_tok, target_tok, parent, cu_nodes, max_path):
+    """Greedy acceptance oracle (plain loops); see ``replay.accept_greedy``."""
+    return replay.accept_greedy(draft_tok, target_tok, parent, cu_nodes, max_path)
 
 
 def batch_inputs(tb):

@@ -112,3 +112,42 @@ def commit(ST0, k, v, beta, g, parent, cu_nodes, path, path_len):
                 S, _ = rule_step(S, float(np.exp(g[j, h])), float(beta[j, h]), k[j, h], v[j, h])
             out[r, h] = S.T
     return out
+
+
+def accept_greedy(draft_tok, target_tok, parent, cu_nodes, max_path):
+    """Greedy acceptance (GDN Tree-Scan abstract: device-side commitment of the accepted chain;
+    TreeWY page, method section: outputs decide acceptance, then the accepted path is committed).
+
+    Per request: start at node 0 (the root, always kept); at node x move to the lowest-indexed
+    child c with draft_tok[c] == target_tok[x]; stop when no child matches or max_path nodes are
+    taken. Returns (path [B, max_path] int32 padded with -1, path_len [B] int32, truncated [B] bool).
+    Malformed trees (parent[t] outside [-1, t-1]) raise ValueError.
+    """
+    parent = np.asarray(parent)
+    cu_nodes = np.asarray(cu_nodes)
+    _check_tree(parent, cu_nodes)
+    B = len(cu_nodes) - 1
+    path = np.full((B, max_path), -1, dtype=np.int32)
+    path_len = np.zeros(B, dtype=np.int32)
+    truncated = np.zeros(B, dtype=bool)
+    for r in range(B):
+        t0, n = int(cu_nodes[r]), int(cu_nodes[r + 1] - cu_nodes[r])
+        if n == 0:
+            continue
+        if max_path == 0:
+            truncated[r] = True
+            continue
+        seq = [0]
+        x = 0
+        while True:
+            match = [c for c in range(x + 1, n) if parent[t0 + c] == x and draft_tok[t0 + c] == target_tok[t0 + x]]
+            if not match:
+                break
+            if len(seq) == max_path:
+                truncated[r] = True
+                break
+            x = match[0]
+            seq.append(x)
+        path[r, :len(seq)] = seq
+        path_len[r] = len(seq)
+    return path, path_len, truncated

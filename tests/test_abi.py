@@ -8,7 +8,7 @@ import pytest
 from gated_deltanet_tree_03_b300 import binding as gb
 
 EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_tree_verify_storeall",
-            "gdn_tree_commit_storeall", "gdn_status_str", "gdn_abi_version"}
+            "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_status_str", "gdn_abi_version"}
 
 
 def test_header_declares_expected_symbols():
@@ -70,3 +70,17 @@ def test_binding_raises_on_error():
         gb.gdn_tree_verify(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 4, 48, 32, 4, FAKE, FAKE, FAKE,
                            stream=0)
     assert e.value.code == gb.GDN_EINVAL
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(max_path=65), gb.GDN_ETOOBIG), (dict(max_nodes=65), gb.GDN_ETOOBIG), (dict(B=-1), gb.GDN_EINVAL),
+    (dict(path=None), gb.GDN_EINVAL), (dict(draft=None), gb.GDN_EINVAL), (dict(path_len=FAKE + 4), gb.GDN_EALIGN),
+    (dict(B=0), gb.GDN_OK)])
+def test_accept_host_checks(kw, code):
+    args = dict(draft=FAKE, target=FAKE, parent=FAKE, cu_nodes=FAKE, B=1, T=4, max_nodes=4, max_path=4, path=FAKE,
+                path_len=FAKE, status=None)
+    args.update(kw)
+    rc = gb.library().gdn_tree_accept_greedy(*[args[x] for x in ("draft", "target", "parent", "cu_nodes", "B", "T",
+                                                                 "max_nodes", "max_path", "path", "path_len",
+                                                                 "status")], None)
+    assert rc == code
