@@ -60,6 +60,13 @@ def commit_bytes(tb) -> int:
     return active * tb.H * 2 * tb.dk * tb.dv * 4 + int(L.sum()) * tb.H * (tb.dv * 4 + tb.dk * 2 + 4)
 
 
+def fused_bytes(tb) -> int:
+    """gdn_tree_commit_verify with the same tree on both sides of the step: the verify's and the
+    commit's bytes, less the one state read the fusion removes per committed (request, head)."""
+    active = int(np.sum(tb.path_len.astype(np.int64) > 0))
+    return verify_bytes(tb) + commit_bytes(tb) - active * tb.H * tb.dk * tb.dv * 4
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -356,6 +363,47 @@ def run_ours(args):
         "verify+commit": {"ms": v_ms + c_ms, "GB/s": (vb + cb) / ((v_ms + c_ms) * 1e6),
                           "frac": (vb + cb) / ((v_ms + c_ms) * 1e6) / peaks["hbm_gbs"]},
     }
+    if args.fused:
+        # deferred commit: every step commits the previous step's accepted paths and verifies the
+        # next trees in one gdn_tree_commit_verify call (same inputs on both sides of the step;
+        # the previous step's pseudo-values and log-gates alternate between two buffers per layer)
+        nl = len(layers)
+        pv = [[(torch.empty_like(o["U"]), torch.empty_like(o["G"])) for _ in range(2)] for o in dev_out]
+        for j in range(nl):
+            tb, d, o = layers[j], dev_in[j], dev_out[j]
+            gb.gdn_tree_verify(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], tb.B,
+                               tb.H, tb.T, tb.dk, tb.dv, tb.max_nodes, o["o"], pv[j][0][0], pv[j][0][1], o["status"],
+                               stream)
+        cur = [0] * nl
+
+        def fused_step(i):
+            j = i % nl
+            tb, d, o = layers[j], dev_in[j], dev_out[j]
+            (Up, Gp), (Un, Gn) = pv[j][cur[j]], pv[j][1 - cur[j]]
+            gb.gdn_tree_commit_verify(d["ST"], Up, Gp, d["k"], d["parent"], d["cu_nodes"], d["path"], d["path_len"],
+                                      tb.T, tb.max_path, d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"],
+                                      d["cu_nodes"], tb.B, tb.H, tb.T, tb.dk, tb.dv, tb.max_nodes, o["o"], Un, Gn,
+                                      o["status"], stream)
+            cur[j] = 1 - cur[j]
+
+        for i in range(args.warmup):
+            fused_step(i)
+        torch.cuda.synchronize()
+        if sum(int(o["status"][0].item()) for o in dev_out):
+            raise RuntimeError("device reported data errors in the fused steps")
+        if dist is not None:
+            dist.barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(K):
+            fused_step(i)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        f_ms = max_over_ranks(dist, f0.elapsed_time(f1), dev) / K
+        fb = float(np.mean([fused_bytes(tb) for tb in layers]))
+        kernels["commit_verify"] = {"ms": f_ms, "alg_bytes": fb, "GB/s": fb / (f_ms * 1e6),
+                                    "frac": fb / (f_ms * 1e6) / peaks["hbm_gbs"],
+                                    "node_verifications_per_s": nodes_per_step * world / (f_ms / 1e3)}
     for kd in kernels.values():
         kd["frac_of_nominal"] = kd["GB/s"] / NOMINAL_HBM_GBS
     dom = "verify" if v_ms >= c_ms else "commit"
@@ -436,6 +484,12 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (per-layer state > 126 MB; layers rotated)",
                        "parallelism": f"dp{world} (independent batches per GPU)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clk,
+            "fused_commit_verify": None if "commit_verify" not in kernels else {
+                "value": kernels["commit_verify"]["node_verifications_per_s"], "unit": UNIT,
+                "ms_per_step": kernels["commit_verify"]["ms"], "achieved_GBps": kernels["commit_verify"]["GB/s"],
+                "frac": kernels["commit_verify"]["frac"], "steps": K, "gpu_launches": K,
+                "note": "gdn_tree_commit_verify: each step commits the previous step's accepted paths and verifies "
+                        "the next trees in one pass over the state (deferred commit); same work as verify + commit"},
             "kernels": kernels, "wall_s_timed": wall}
     if rank == 0:
         print(json.dumps(line))
@@ -458,6 +512,8 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-fused", dest="fused", action="store_false",
+                    help="skip timing gdn_tree_commit_verify (the previous step's commit folded into the next verify)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

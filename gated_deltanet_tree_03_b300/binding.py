@@ -46,6 +46,7 @@ _SIGS = {
     "gdn_tree_verify_storeall": [_P] * 8 + [_I] * 6 + [_P] * 5 + [_P],
     "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 6 + [_P, _P],
     "gdn_tree_accept_greedy": [_P] * 4 + [_I] * 4 + [_P] * 3 + [_P],
+    "gdn_tree_commit_verify": [_P] * 8 + [_I] * 2 + [_P] * 7 + [_I] * 6 + [_P] * 4 + [_P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -147,3 +148,13 @@ def gdn_tree_accept_greedy(draft_tok, target_tok, parent, cu_nodes, B, T, max_no
     _check(_lib.gdn_tree_accept_greedy(_ptr(draft_tok), _ptr(target_tok), _ptr(parent), _ptr(cu_nodes), B, T,
                                        max_nodes, max_path, _ptr(path), _ptr(path_len), _ptr(status),
                                        _stream(stream)), "gdn_tree_accept_greedy")
+
+
+def gdn_tree_commit_verify(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path,
+                           q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status=None,
+                           stream=None):
+    _check(_lib.gdn_tree_commit_verify(_ptr(ST), _ptr(U_prev), _ptr(G_prev), _ptr(k_prev), _ptr(parent_prev),
+                                       _ptr(cu_nodes_prev), _ptr(path), _ptr(path_len), T_prev, max_path, _ptr(q),
+                                       _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent), _ptr(cu_nodes), B, H, T,
+                                       d_k, d_v, max_nodes, _ptr(o), _ptr(U), _ptr(G), _ptr(status),
+                                       _stream(stream)), "gdn_tree_commit_verify")

@@ -166,18 +166,30 @@ gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
   return launch_status();
 }
 
-template <int DK, int DV, int NMAX>
-gdn_status launch_verify_stream(const VerifyArgs &a, cudaStream_t stream) {
+template <int DK, int DV, int NMAX, bool FUSE>
+gdn_status launch_verify_stream(const VerifyArgs &a, const PrevCommit &c, cudaStream_t stream) {
   const long long blocks = (long long)a.B * a.H;
-  verify_stream_kernel<DK, DV, NMAX><<<unsigned(blocks), DV / 2, 0, stream>>>(a);
+  verify_stream_kernel<DK, DV, NMAX, FUSE><<<unsigned(blocks), DV / 2, 0, stream>>>(a, c);
   return launch_status();
 }
 
-template <int DK, int DV>
-gdn_status launch_verify_stream_n(const VerifyArgs &a, cudaStream_t stream) {
-  if (a.max_nodes <= 4) return launch_verify_stream<DK, DV, 4>(a, stream);
-  if (a.max_nodes <= 6) return launch_verify_stream<DK, DV, 6>(a, stream);
-  return launch_verify_stream<DK, DV, 8>(a, stream);
+template <int DK, int DV, bool FUSE>
+gdn_status launch_verify_stream_n(const VerifyArgs &a, const PrevCommit &c, cudaStream_t stream) {
+  if (a.max_nodes <= 4) return launch_verify_stream<DK, DV, 4, FUSE>(a, c, stream);
+  if (a.max_nodes <= 6) return launch_verify_stream<DK, DV, 6, FUSE>(a, c, stream);
+  return launch_verify_stream<DK, DV, 8, FUSE>(a, c, stream);
+}
+
+template <bool FUSE>
+gdn_status launch_verify_stream_dims(const VerifyArgs &a, const PrevCommit &c, cudaStream_t s) {
+  switch (a.dk * 1000 + a.dv) {
+    case 32064: return launch_verify_stream_n<32, 64, FUSE>(a, c, s);
+    case 32128: return launch_verify_stream_n<32, 128, FUSE>(a, c, s);
+    case 64064: return launch_verify_stream_n<64, 64, FUSE>(a, c, s);
+    case 64128: return launch_verify_stream_n<64, 128, FUSE>(a, c, s);
+    case 128064: return launch_verify_stream_n<128, 64, FUSE>(a, c, s);
+    default: return launch_verify_stream_n<128, 128, FUSE>(a, c, s);
+  }
 }
 
 template <int DK, int DV>
@@ -250,16 +262,8 @@ gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k
   if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
   VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (max_nodes <= kStreamMaxNodes) {  // small trees: CUDA-core streaming kernel
-    switch (d_k * 1000 + d_v) {
-      case 32064: return launch_verify_stream_n<32, 64>(a, s);
-      case 32128: return launch_verify_stream_n<32, 128>(a, s);
-      case 64064: return launch_verify_stream_n<64, 64>(a, s);
-      case 64128: return launch_verify_stream_n<64, 128>(a, s);
-      case 128064: return launch_verify_stream_n<128, 64>(a, s);
-      default: return launch_verify_stream_n<128, 128>(a, s);
-    }
-  }
+  if (max_nodes <= kStreamMaxNodes)  // small trees: CUDA-core streaming kernel
+    return launch_verify_stream_dims<false>(a, PrevCommit{}, s);
   if (d_k == 128) return d_v == 128 ? launch_verify_tc<128, 128>(a, s) : launch_verify_tc<128, 64>(a, s);
   return d_v == 128 ? launch_verify_tc<64, 128>(a, s) : launch_verify_tc<64, 64>(a, s);
 }
@@ -306,6 +310,38 @@ gdn_status gdn_tree_accept_greedy(const int32_t *draft_tok, const int32_t *targe
   const unsigned blocks = unsigned((B + kAcceptWarps - 1) / kAcceptWarps);
   accept_greedy_kernel<<<blocks, kAcceptWarps * 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
+}
+
+gdn_status gdn_tree_commit_verify(float *ST, const float *U_prev, const float *G_prev,
+                                  const uint16_t *k_prev, const int32_t *parent_prev,
+                                  const int32_t *cu_nodes_prev, const int32_t *path,
+                                  const int32_t *path_len, int32_t T_prev, int32_t max_path,
+                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                  const float *beta, const float *g, const int32_t *parent,
+                                  const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
+                                  int32_t d_k, int32_t d_v, int32_t max_nodes, float *o, float *U,
+                                  float *G, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_commit_args(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H,
+                                    T_prev, d_k, d_v, max_path, status);
+  if (st != GDN_OK) return st;
+  if ((st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G,
+                              status)) != GDN_OK)
+    return st;
+  if (B == 0) return GDN_OK;
+  if (U && U == U_prev) return GDN_EINVAL;  // this step's pseudo-values may not overwrite the previous ones
+  const bool fusable = T > 0 && d_v != 32 && max_nodes <= kStreamMaxNodes && max_path <= kFuseMaxPath;
+  if (!fusable) {  // the same result from the two kernels in order
+    if ((st = gdn_tree_commit(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H, T_prev,
+                              d_k, d_v, max_path, status, stream)) != GDN_OK)
+      return st;
+    return gdn_tree_verify(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status,
+                           stream);
+  }
+  if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
+  PrevCommit c{ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path};
+  return launch_verify_stream_dims<true>(a, c, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,

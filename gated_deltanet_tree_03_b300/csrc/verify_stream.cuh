@@ -16,6 +16,11 @@
 // dot products. At N <= 8 the 4 N d_k d_v FMAs per pair stay below the time the pair's state
 // takes to arrive from HBM, so the kernel is bandwidth-bound without tensor cores or any
 // shared-memory round trip of the state.
+//
+// With FUSE the kernel first folds the previous step's accepted path into each state row as it
+// streams past (the commit update ST <- exp(G_l) ST + sum_j exp(G_l - G_j) k_j u_j^T of that path),
+// writes the row back once, and projects the updated row: commit and the next verify then read
+// and write every state element once between them instead of reading it twice.
 #pragma once
 
 #include "common.cuh"
@@ -31,20 +36,36 @@ __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
 
 // Register cap per thread, sized so that 14 (four nodes), 11 (six) or 9 (eight) 64-thread CTAs
 // share an SM.
-__host__ __device__ constexpr int stream_max_regs(int nmax) { return nmax <= 4 ? 72 : nmax <= 6 ? 88 : 112; }
+__host__ __device__ constexpr int stream_max_regs(int nmax, bool fuse) {
+  return fuse ? (nmax <= 4 ? 96 : nmax <= 6 ? 112 : 128) : (nmax <= 4 ? 72 : nmax <= 6 ? 88 : 112);
+}
+
+constexpr int kFuseMaxPath = 4;  // accepted-path entries the fused kernel folds in (u_j kept in registers)
+
+// The previous step's accepted path, folded into the state by the fused kernel.
+struct PrevCommit {
+  float *ST;  // the same array as VerifyArgs::ST, written in place
+  const float *U, *G;
+  const uint16_t *k;
+  const int32_t *parent, *cu_nodes, *path, *path_len;
+  int T, max_path;
+};
 
 // State rows each thread keeps in flight (more rows cost resident CTAs; 16 measured best).
 __host__ __device__ constexpr int stream_prefetch_rows(int) { return 16; }
 
-template <int DK, int DV, int NMAX>
-__global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) verify_stream_kernel(VerifyArgs a) {
+template <int DK, int DV, int NMAX, bool FUSE>
+__global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE))
+    verify_stream_kernel(VerifyArgs a, PrevCommit c) {
   constexpr int NT = DV / 2;    // threads
   constexpr int NW = NT / 32;   // warps
   constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
   constexpr int DV2 = DV / 2;   // float2 per state row
   constexpr int kStreamPF = stream_prefetch_rows(NMAX);
+  constexpr int LW = FUSE ? kFuseMaxPath : 1;
   static_assert(NMAX <= 8 && DK % kStreamPF == 0 && NT % 32 == 0, "shape");
   __shared__ __align__(16) float Xs[NX][DK];
+  __shared__ __align__(16) float Ws[LW][DK];  // fused: exp(G_l - G_j) k_j per accepted-path entry
   __shared__ float Ac[NMAX][NMAX], Pc[NMAX][NMAX];
   __shared__ float G_s[NMAX], gam_s[NMAX], beta_s[NMAX], g_s[NMAX];
   __shared__ int par_s[NMAX];
@@ -60,22 +81,63 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
 #pragma unroll
   for (int i = 0; i < kStreamPF; ++i) s[i] = __ldcs(st + i * DV2);
 
-  // 2) request bounds and checks
+  // 2) request bounds and checks (uniform across the CTA)
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
+  bool vok = true;
   if (!offsets_ok(t0, n, a.T)) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
-    return;
-  }
-  if (n == 0) return;
-  if (n > a.max_nodes || n > NMAX) {
+    vok = false;
+  } else if (n == 0) {
+    vok = false;
+  } else if (n > a.max_nodes || n > NMAX) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
-    return;
+    vok = false;
   }
   const int H = a.H;
 
+  // 2b) fused: the previous step's accepted path (same checks and effect as gdn_tree_commit)
+  int Lc = 0;
+  float decay = 1.f;
+  float2 us[LW];
+#pragma unroll
+  for (int q = 0; q < LW; ++q) us[q] = make_float2(0.f, 0.f);
+  if constexpr (FUSE) {
+    const int L = c.path_len[r];
+    const int tp0 = c.cu_nodes[r];
+    const int np = c.cu_nodes[r + 1] - tp0;
+    bool cok = L != 0;
+    if (cok && !offsets_ok(tp0, np, c.T)) {
+      if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
+      cok = false;
+    }
+    if (cok && (L < 0 || L > np || L > c.max_path || L > kFuseMaxPath)) {
+      if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
+      cok = false;
+    }
+    const int32_t *path_r = c.path + size_t(r) * c.max_path;
+    if (cok && !check_path(c.parent, path_r, tp0, np, L, c.max_path)) {
+      if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
+      cok = false;
+    }
+    if (cok) {
+      const float Gl = c.G[size_t(tp0 + path_r[L - 1]) * H + h];
+      decay = expf(Gl);
+      for (int i = tid; i < L * DK; i += NT) {
+        const int q = i / DK, row = i % DK;
+        const size_t th = size_t(tp0 + path_r[q]) * H + h;
+        Ws[q][row] = expf(Gl - c.G[th]) * bf16_to_f32(c.k[th * DK + row]);
+      }
+#pragma unroll
+      for (int q = 0; q < LW; ++q)
+        if (q < L) us[q] = reinterpret_cast<const float2 *>(c.U + (size_t(tp0 + path_r[q]) * H + h) * DV)[col2];
+      Lc = L;
+    }
+  }
+  if (!vok && Lc == 0) return;  // nothing to fold in and nothing to verify
+
   // 3) node block (fp32, rows >= n zero), this thread's v pairs, tree inputs
-  for (int i = tid; i < NX * DK / 4; i += NT) {
+  for (int i = tid; vok && i < NX * DK / 4; i += NT) {
     const int row = i / (DK / 4), c4 = i % (DK / 4);
     const int t = row < NMAX ? row : row - NMAX;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -90,9 +152,9 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
   uint32_t vb[NMAX];
 #pragma unroll
   for (int t = 0; t < NMAX; ++t)
-    vb[t] = t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
+    vb[t] = vok && t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
   int bad = 0;
-  if (tid < n) {
+  if (vok && tid < n) {
     const int p = a.parent[t0 + tid];
     bad = (p < -1 || p >= tid);
     par_s[tid] = p;
@@ -101,9 +163,10 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
-    return;
+    vok = false;
+    if (Lc == 0) return;
   }
-  if (tid < n) {
+  if (vok && tid < n) {
     // parent indices strictly decrease along the walk, so it ends within tid + 1 steps
     uint32_t m = 1u << tid;
     float Gs = g_s[tid];
@@ -121,7 +184,10 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
   float2 acc[NX];
 #pragma unroll
   for (int t = 0; t < NX; ++t) acc[t] = make_float2(0.f, 0.f);
-#pragma unroll
+  // the fused kernel keeps the block loop rolled: unrolled, the fold's coefficient loads are
+  // hoisted across blocks and the register count doubles
+  constexpr int KUNROLL = FUSE ? 1 : DK / kStreamPF;
+#pragma unroll KUNROLL
   for (int k0 = 0; k0 < DK; k0 += kStreamPF) {
     float2 nx[kStreamPF];
     if (k0 + kStreamPF < DK) {
@@ -130,6 +196,30 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
     }
 #pragma unroll
     for (int g4 = 0; g4 < kStreamPF; g4 += 4) {
+      if constexpr (FUSE) {
+        if (Lc > 0) {  // fold the accepted path into these four rows and write them back once
+          float2 *stw = reinterpret_cast<float2 *>(c.ST + size_t(pair) * DK * DV) + col2;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[g4 + i] = make_float2(decay * s[g4 + i].x, decay * s[g4 + i].y);
+#pragma unroll
+          for (int q = 0; q < LW; ++q) {
+            if (q < Lc) {
+              const float4 w = *reinterpret_cast<const float4 *>(&Ws[q][k0 + g4]);
+              s[g4].x = fmaf(w.x, us[q].x, s[g4].x);
+              s[g4].y = fmaf(w.x, us[q].y, s[g4].y);
+              s[g4 + 1].x = fmaf(w.y, us[q].x, s[g4 + 1].x);
+              s[g4 + 1].y = fmaf(w.y, us[q].y, s[g4 + 1].y);
+              s[g4 + 2].x = fmaf(w.z, us[q].x, s[g4 + 2].x);
+              s[g4 + 2].y = fmaf(w.z, us[q].y, s[g4 + 2].y);
+              s[g4 + 3].x = fmaf(w.w, us[q].x, s[g4 + 3].x);
+              s[g4 + 3].y = fmaf(w.w, us[q].y, s[g4 + 3].y);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) __stcs(stw + (k0 + g4 + i) * DV2, s[g4 + i]);
+        }
+        if (!vok) continue;
+      }
 #pragma unroll
       for (int t = 0; t < NX; ++t) {
         const float4 x = *reinterpret_cast<const float4 *>(&Xs[t][k0 + g4]);
@@ -148,6 +238,8 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX)) ver
       for (int i = 0; i < kStreamPF; ++i) s[i] = nx[i];
     }
   }
+
+  if (!vok) return;
 
   // 5) masked, gated Gram entries: one warp per (t, j) entry, lanes split d_k
   {

@@ -132,6 +132,38 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
                            gdn_stream_t stream);
 
 /*
+ * gdn_tree_commit_verify - gdn_tree_commit of the previous step's accepted path followed by
+ * gdn_tree_verify of this step's tree, on the same state, in one pass where the shapes allow.
+ *
+ * In a decode loop a layer's commit for step i and its verify for step i+1 touch the same state
+ * back to back. Deferring the commit to the next verify lets one kernel fold the accepted path
+ * into each state row as it streams in (TreeWY page, method section: only the accepted path's
+ * pseudo-values rebuild the next committed state), write the row back once and project the
+ * updated row against the new tree: each state element is read once and written once for the
+ * pair of operations instead of read twice. Results equal gdn_tree_commit then gdn_tree_verify.
+ *
+ *   ST                               in/out  committed state; updated in place
+ *   U_prev, G_prev, k_prev,          in      the previous step's pseudo-values, cumulative
+ *   parent_prev, cu_nodes_prev,              log-gates, keys and tree (as for gdn_tree_commit),
+ *   path, path_len, T_prev, max_path         and its accepted paths
+ *   q, k, v, beta, g, parent,        in      this step's tree (as for gdn_tree_verify)
+ *   cu_nodes, B, H, T, d_k, d_v, max_nodes
+ *   o, U, G                          out     this step's outputs; U must not alias U_prev
+ *   status                           out     optional, bits of both operations
+ * One fused kernel runs when d_v is 64 or 128, max_nodes <= 8 and max_path <= 8; otherwise the
+ * two kernels run in order on `stream`, with the same result.
+ */
+gdn_status gdn_tree_commit_verify(float *ST, const float *U_prev, const float *G_prev,
+                                  const uint16_t *k_prev, const int32_t *parent_prev,
+                                  const int32_t *cu_nodes_prev, const int32_t *path,
+                                  const int32_t *path_len, int32_t T_prev, int32_t max_path,
+                                  const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                  const float *beta, const float *g, const int32_t *parent,
+                                  const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
+                                  int32_t d_k, int32_t d_v, int32_t max_nodes, float *o, float *U,
+                                  float *G, int32_t *status, gdn_stream_t stream);
+
+/*
  * gdn_tree_verify_storeall - the comparison baseline the TreeWY page calls "storeall"
  * (comparison with prior methods): step every node from its parent's stored state in
  * topological order and store the state at every node.

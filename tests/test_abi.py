@@ -8,7 +8,8 @@ import pytest
 from gated_deltanet_tree_03_b300 import binding as gb
 
 EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_tree_verify_storeall",
-            "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_status_str", "gdn_abi_version"}
+            "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_tree_commit_verify", "gdn_status_str",
+            "gdn_abi_version"}
 
 
 def test_header_declares_expected_symbols():
