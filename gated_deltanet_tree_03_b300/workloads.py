@@ -4,19 +4,19 @@ This module only *draws* inputs. It holds none of the method's arithmetic
 (no recurrence, no solve, no commit), so the CPU oracle and the CUDA path can
 both be fed from it without sharing any computation.
 
-Workloads (sizes, shapes and distributions) follow the synthetic
-configurations the TreeWY and GDN Tree-Scan pages motivate:
+Workload presets (``make_config(i)``; sizes, shapes and distributions of the synthetic
+workloads the TreeWY and GDN Tree-Scan pages motivate):
 
-* config 0 - one request, one head, d=32, a chain of 3 draft nodes, path = first 2.
-* config 1 - depth-3 chain (bonus + 3 drafts = 4 nodes), 256 requests, 32 heads,
-  d=128 (the "depth-3 chain" setting of the TreeWY page, experiments section).
-* config 2 - the 6-node root-branch tree of the GDN Tree-Scan abstract
-  (root with 3 children, 2 of them with one child each), batch 1 or 64, 48 heads.
-* config 3 - random trees of 16..64 nodes (fanout 1..4, depth <= 8), batch 128.
-* config 4 - 32-node random trees (fanout 1..3, depth <= 6), gate a ~ U(0.85, 1),
+* 0 - one request, one head, d=32, a chain of 3 draft nodes, accepted path = first 2.
+* 1 - depth-3 chain (bonus + 3 drafts = 4 nodes), 256 requests, 32 heads, d=128
+  (the "depth-3 chain" setting of the TreeWY page, experiments section).
+* 2 - the 6-node root-branch tree of the GDN Tree-Scan abstract (root with 3
+  children, 2 of them with one child each), batch 1 or 64, 48 heads.
+* 3 - ragged random trees of 16..64 nodes (fanout 1..4, depth <= 8), batch 128.
+* 4 - 32-node random trees (fanout 1..3, depth <= 6), gate a ~ U(0.85, 1),
   batch 1..512, 32 heads, one independent input set per GDN layer.
 
-Value recipe (all configs): state S ~ N(0, 0.1^2) in fp32; q, k ~ N(0, 1) drawn in
+Value recipe (all presets): state S ~ N(0, 0.1^2) in fp32; q, k ~ N(0, 1) drawn in
 fp32, L2-normalised in fp32, then rounded to bf16 (round-to-nearest-even);
 v ~ N(0, 1) rounded to bf16; beta ~ U(0, 1) fp32; gate a = exp(-0.1*softplus(x)),
 x ~ N(0, 1), passed as the natural log g = ln a (fp32).
@@ -294,9 +294,9 @@ CONFIG_LAYERS = {0: 1, 1: 1, 2: 1, 3: 1, 4: 48}
 
 
 def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int | None = None) -> TreeBatch:
-    """Build one layer of synthetic config ``idx`` (0..4).
+    """Build one layer of workload preset ``idx`` (0..4, see the module docstring).
 
-    ``batch`` picks one of the config's batch sizes (default: the largest listed);
+    ``batch`` picks one of the preset's batch sizes (default: the largest listed);
     ``heads`` may shrink the head count for quick tests (same per-head distributions).
     """
     if batch is None:
@@ -306,7 +306,7 @@ def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int |
     if idx == 0:
         parents = [chain_parents(3)]
         paths = [[0, 1]]
-        return build_batch(rng, parents, paths, H=heads or 1, dk=32, dv=32, name="config0_chain3_d32")
+        return build_batch(rng, parents, paths, H=heads or 1, dk=32, dv=32, name="chain3_d32")
     if idx == 1:
         parents, paths = [], []
         for _ in range(batch):
@@ -314,7 +314,7 @@ def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int |
             L = int(rng.integers(0, 4))  # accepted drafts after the always-committed bonus node
             paths.append(list(range(L + 1)))
         return build_batch(rng, parents, paths, H=heads or 32, dk=128, dv=128,
-                           name=f"config1_chain4_B{batch}")
+                           name=f"chain4_B{batch}")
     if idx == 2:
         parents, paths = [], []
         for _ in range(batch):
@@ -322,7 +322,7 @@ def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int |
             parents.append(p)
             paths.append(greedy_walk_path(rng, p))
         return build_batch(rng, parents, paths, H=heads or 48, dk=128, dv=128,
-                           name=f"config2_rootbranch6_B{batch}")
+                           name=f"rootbranch6_B{batch}")
     if idx == 3:
         parents, paths = [], []
         for _ in range(batch):
@@ -331,7 +331,7 @@ def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int |
             parents.append(p)
             paths.append(leaf_prefix_path(rng, p))
         return build_batch(rng, parents, paths, H=heads or 32, dk=128, dv=128,
-                           name=f"config3_ragged16to64_B{batch}")
+                           name=f"ragged16to64_B{batch}")
     if idx == 4:
         parents, paths = [], []
         for _ in range(batch):
@@ -339,7 +339,7 @@ def make_config(idx: int, batch: int | None = None, layer: int = 0, heads: int |
             parents.append(p)
             paths.append(leaf_prefix_path(rng, p))
         return build_batch(rng, parents, paths, H=heads or 32, dk=128, dv=128, gate="uniform",
-                           name=f"config4_tree32_B{batch}_layer{layer}")
+                           name=f"tree32_B{batch}_layer{layer}")
     raise ValueError(f"unknown config {idx}")
 
 
