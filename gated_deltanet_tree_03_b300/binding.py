@@ -17,7 +17,7 @@ from . import _build
 
 GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
 STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8, 16
-STATUS_PATH_TRUNCATED = 32
+STATUS_PATH_TRUNCATED, STATUS_BAD_SLOT = 32, 64
 MAX_NODES = 64
 
 HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
@@ -39,6 +39,16 @@ _lib = _load()
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
 
+
+class GdnLayout(ctypes.Structure):
+    """``gdn_layout`` of gdn_tree.h (serving layout of the *_ex entry points)."""
+
+    _fields_ = [("state_slot", _P), ("n_slots", _I), ("H_qk", _I), ("q_scale", ctypes.c_float),
+                ("a_raw", _P), ("b_raw", _P), ("A_log", _P), ("dt_bias", _P)]
+
+
+_LP = ctypes.POINTER(GdnLayout)
+
 _SIGS = {
     "gdn_tree_verify": [_P] * 8 + [_I] * 6 + [_P] * 4 + [_P],
     "gdn_tree_verify_simt": [_P] * 8 + [_I] * 6 + [_P] * 4 + [_P],
@@ -47,6 +57,9 @@ _SIGS = {
     "gdn_tree_commit_storeall": [_P] * 6 + [_I] * 6 + [_P, _P],
     "gdn_tree_accept_greedy": [_P] * 4 + [_I] * 4 + [_P] * 3 + [_P],
     "gdn_tree_commit_verify": [_P] * 8 + [_I] * 2 + [_P] * 7 + [_I] * 6 + [_P] * 4 + [_P],
+    "gdn_tree_verify_ex": [_P] * 8 + [_I] * 6 + [_LP] + [_P] * 4 + [_P],
+    "gdn_tree_commit_ex": [_P] * 8 + [_I] * 6 + [_LP] + [_P, _P],
+    "gdn_tree_commit_verify_ex": [_P] * 8 + [_I] * 2 + [_P] * 7 + [_I] * 6 + [_LP] + [_P] * 4 + [_P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -158,3 +171,37 @@ def gdn_tree_commit_verify(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_pre
                                        _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent), _ptr(cu_nodes), B, H, T,
                                        d_k, d_v, max_nodes, _ptr(o), _ptr(U), _ptr(G), _ptr(status),
                                        _stream(stream)), "gdn_tree_commit_verify")
+
+
+def layout(state_slot=None, n_slots=0, H_qk=0, q_scale=1.0, a_raw=None, b_raw=None, A_log=None, dt_bias=None):
+    """A ``GdnLayout`` from device arrays (torch CUDA tensors or addresses) and scalars."""
+    return GdnLayout(_ptr(state_slot), int(n_slots), int(H_qk), float(q_scale), _ptr(a_raw), _ptr(b_raw),
+                     _ptr(A_log), _ptr(dt_bias))
+
+
+def _lay(lay):
+    return None if lay is None else ctypes.byref(lay)
+
+
+def gdn_tree_verify_ex(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, lay, o, U, G,
+                       status=None, stream=None):
+    _check(_lib.gdn_tree_verify_ex(_ptr(ST), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent),
+                                   _ptr(cu_nodes), B, H, T, d_k, d_v, max_nodes, _lay(lay), _ptr(o), _ptr(U),
+                                   _ptr(G), _ptr(status), _stream(stream)), "gdn_tree_verify_ex")
+
+
+def gdn_tree_commit_ex(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, lay,
+                       status=None, stream=None):
+    _check(_lib.gdn_tree_commit_ex(_ptr(ST), _ptr(U), _ptr(G), _ptr(k), _ptr(parent), _ptr(cu_nodes), _ptr(path),
+                                   _ptr(path_len), B, H, T, d_k, d_v, max_path, _lay(lay), _ptr(status),
+                                   _stream(stream)), "gdn_tree_commit_ex")
+
+
+def gdn_tree_commit_verify_ex(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev,
+                              max_path, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, lay, o, U,
+                              G, status=None, stream=None):
+    _check(_lib.gdn_tree_commit_verify_ex(_ptr(ST), _ptr(U_prev), _ptr(G_prev), _ptr(k_prev), _ptr(parent_prev),
+                                          _ptr(cu_nodes_prev), _ptr(path), _ptr(path_len), T_prev, max_path, _ptr(q),
+                                          _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent), _ptr(cu_nodes), B, H,
+                                          T, d_k, d_v, max_nodes, _lay(lay), _ptr(o), _ptr(U), _ptr(G), _ptr(status),
+                                          _stream(stream)), "gdn_tree_commit_verify_ex")

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/gdn_tree.h: argument checks, launch
 // configuration, TMA descriptor encoding and kernel dispatch. Nothing here allocates device
 // memory, synchronises the device or keeps per-call state.
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -49,17 +50,20 @@ gdn_status check_verify_args(const float *ST, const uint16_t *q, const uint16_t 
                              const uint16_t *v, const float *beta, const float *g,
                              const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H,
                              int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes, const float *o,
-                             const float *U, const float *G, const int32_t *status) {
+                             const float *U, const float *G, const int32_t *status,
+                             const Serving &L = Serving{}) {
   if (B < 0 || H <= 0 || T < 0 || max_nodes < 0) return GDN_EINVAL;
   if (B > 65535 || H > 65535) return GDN_EINVAL;  // grid limits
   if (!valid_d(d_k) || !valid_d(d_v)) return GDN_EINVAL;
   if (max_nodes > kMaxNodes) return GDN_ETOOBIG;
   if (B == 0 || T == 0) return GDN_OK;
-  if (!ST || !q || !k || !v || !beta || !g || !parent || !cu_nodes || !o || !U || !G)
-    return GDN_EINVAL;
-  const void *ptrs[] = {ST, q, k, v, beta, g, parent, cu_nodes, o, U, G};
+  const bool fused_gates = L.a_raw != nullptr;  // beta and g are then formed in the kernels
+  if (!ST || !q || !k || !v || !parent || !cu_nodes || !o || !U || !G) return GDN_EINVAL;
+  if (!fused_gates && (!beta || !g)) return GDN_EINVAL;
+  const void *ptrs[] = {ST, q, k, v, parent, cu_nodes, o, U, G};
   for (const void *p : ptrs)
     if (!aligned16(p)) return GDN_EALIGN;
+  if (!fused_gates && (!aligned16(beta) || !aligned16(g))) return GDN_EALIGN;
   if (status && !aligned16(status)) return GDN_EALIGN;
   return GDN_OK;
 }
@@ -78,6 +82,37 @@ gdn_status check_commit_args(const float *ST, const void *a1, const void *a2, co
   const void *ptrs[] = {ST, a1, a2, a3, parent, cu_nodes, path_len, path, status};
   for (const void *p : ptrs)
     if (p && !aligned16(p)) return GDN_EALIGN;
+  return GDN_OK;
+}
+
+// Host checks of a serving layout (gdn_layout, declared in gdn_tree.h) and its kernel form.
+// `full` = a verify call (q_scale and the gate arrays apply); commit reads the slots and H_qk.
+gdn_status make_serving(const gdn_layout *l, int32_t H, bool full, Serving &L) {
+  L = Serving{};
+  if (!l) return GDN_OK;
+  if (H <= 0) return GDN_EINVAL;
+  if (l->H_qk < 0 || (l->H_qk > 0 && H % l->H_qk != 0)) return GDN_EINVAL;
+  L.grp = l->H_qk > 0 ? H / l->H_qk : 1;
+  if (l->state_slot) {
+    if (l->n_slots <= 0) return GDN_EINVAL;
+    if (!aligned16(l->state_slot)) return GDN_EALIGN;
+    L.slot = l->state_slot;
+    L.n_slots = l->n_slots;
+  }
+  if (!full) return GDN_OK;
+  if (!std::isfinite(l->q_scale)) return GDN_EINVAL;
+  L.q_scale = l->q_scale == 0.f ? 1.f : l->q_scale;
+  const int ngate = (l->a_raw != nullptr) + (l->b_raw != nullptr) + (l->A_log != nullptr) + (l->dt_bias != nullptr);
+  if (ngate != 0 && ngate != 4) return GDN_EINVAL;
+  if (ngate == 4) {
+    const void *gp[] = {l->a_raw, l->b_raw, l->A_log, l->dt_bias};
+    for (const void *p : gp)
+      if (!aligned16(p)) return GDN_EALIGN;
+    L.a_raw = l->a_raw;
+    L.b_raw = l->b_raw;
+    L.A_log = l->A_log;
+    L.dt_bias = l->dt_bias;
+  }
   return GDN_OK;
 }
 
@@ -114,15 +149,23 @@ bool encode_rows(CUtensorMap *map, const uint16_t *base, int D, int H, int T, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int DK>
-gdn_status launch_verify_simt(const VerifyArgs &a, cudaStream_t stream) {
+// The plain layout runs the kernels compiled without any serving-layout indexing.
+bool is_plain(const Serving &L) { return !L.slot && L.grp == 1 && L.q_scale == 1.f && !L.a_raw; }
+
+template <int DK, bool SV>
+gdn_status launch_verify_simt_sv(const VerifyArgs &a, const Serving &L, cudaStream_t stream) {
   const size_t smem = verify_simt_smem_bytes(a.max_nodes, DK);
-  if (cudaFuncSetAttribute(verify_simt_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(verify_simt_kernel<DK, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return GDN_ECUDA;
   dim3 grid(a.dv / 32, a.H, a.B);
-  verify_simt_kernel<DK><<<grid, kThreads, smem, stream>>>(a);
+  verify_simt_kernel<DK, SV><<<grid, kThreads, smem, stream>>>(a, L);
   return launch_status();
+}
+
+template <int DK>
+gdn_status launch_verify_simt(const VerifyArgs &a, const Serving &L, cudaStream_t stream) {
+  return is_plain(L) ? launch_verify_simt_sv<DK, false>(a, L, stream) : launch_verify_simt_sv<DK, true>(a, L, stream);
 }
 
 int sm_count() {
@@ -132,19 +175,20 @@ int sm_count() {
   return n;
 }
 
-template <int DK, int DV>
-gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
+template <int DK, int DV, bool SV>
+gdn_status launch_verify_tc_sv(const VerifyArgs &a, const Serving &L, cudaStream_t stream) {
   const int Np = ((a.max_nodes < 1 ? 1 : a.max_nodes) + 15) / 16 * 16;
+  const int HK = a.H / L.grp;  // q/k heads
   CUtensorMap tk, tq, tv;
-  if (!encode_rows(&tk, a.k, DK, a.H, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_rows(&tq, a.q, DK, a.H, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!encode_rows(&tk, a.k, DK, HK, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tq, a.q, DK, HK, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_rows(&tv, a.v, DV, a.H, a.T, DV, Np, CU_TENSOR_MAP_SWIZZLE_NONE))
     return GDN_ECUDA;
   int dev = 0, optin = 0;
   cudaFuncAttributes fa{};
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaFuncGetAttributes(&fa, verify_tc_kernel<DK, DV>) != cudaSuccess)
+      cudaFuncGetAttributes(&fa, verify_tc_kernel<DK, DV, SV>) != cudaSuccess)
     return GDN_ECUDA;
   // deepest state ring that fits next to the node stages (1 KiB slack aligns the base)
   const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024;
@@ -155,52 +199,65 @@ gdn_status launch_verify_tc(const VerifyArgs &a, cudaStream_t stream) {
   // at least ~half an SM's shared memory, so a second CTA never waits on this one's tensor memory
   size_t smem = size_t(lay.total) + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;
-  if (cudaFuncSetAttribute(verify_tc_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(verify_tc_kernel<DK, DV, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(smem)) != cudaSuccess)
     return GDN_ECUDA;
   const long long pairs = (long long)a.B * a.H;
   const int sms = sm_count();
   if (sms <= 0) return GDN_ECUDA;
   const unsigned grid = unsigned(pairs < sms ? pairs : sms);
-  verify_tc_kernel<DK, DV><<<grid, kTcThreads, smem, stream>>>(tk, tq, tv, a, lay);
+  verify_tc_kernel<DK, DV, SV><<<grid, kTcThreads, smem, stream>>>(tk, tq, tv, a, lay, L);
   return launch_status();
 }
 
+template <int DK, int DV>
+gdn_status launch_verify_tc(const VerifyArgs &a, const Serving &L, cudaStream_t stream) {
+  return is_plain(L) ? launch_verify_tc_sv<DK, DV, false>(a, L, stream) : launch_verify_tc_sv<DK, DV, true>(a, L, stream);
+}
+
 template <int DK, int DV, int NMAX, bool FUSE>
-gdn_status launch_verify_stream(const VerifyArgs &a, const PrevCommit &c, cudaStream_t stream) {
+gdn_status launch_verify_stream(const VerifyArgs &a, const PrevCommit &c, const Serving &L, cudaStream_t stream) {
   const long long blocks = (long long)a.B * a.H;
-  verify_stream_kernel<DK, DV, NMAX, FUSE><<<unsigned(blocks), DV / 2, 0, stream>>>(a, c);
+  if (is_plain(L))
+    verify_stream_kernel<DK, DV, NMAX, FUSE, false><<<unsigned(blocks), DV / 2, 0, stream>>>(a, c, L);
+  else
+    verify_stream_kernel<DK, DV, NMAX, FUSE, true><<<unsigned(blocks), DV / 2, 0, stream>>>(a, c, L);
   return launch_status();
 }
 
 template <int DK, int DV, bool FUSE>
-gdn_status launch_verify_stream_n(const VerifyArgs &a, const PrevCommit &c, cudaStream_t stream) {
-  if (a.max_nodes <= 4) return launch_verify_stream<DK, DV, 4, FUSE>(a, c, stream);
-  if (a.max_nodes <= 6) return launch_verify_stream<DK, DV, 6, FUSE>(a, c, stream);
-  return launch_verify_stream<DK, DV, 8, FUSE>(a, c, stream);
+gdn_status launch_verify_stream_n(const VerifyArgs &a, const PrevCommit &c, const Serving &L, cudaStream_t stream) {
+  if (a.max_nodes <= 4) return launch_verify_stream<DK, DV, 4, FUSE>(a, c, L, stream);
+  if (a.max_nodes <= 6) return launch_verify_stream<DK, DV, 6, FUSE>(a, c, L, stream);
+  return launch_verify_stream<DK, DV, 8, FUSE>(a, c, L, stream);
 }
 
 template <bool FUSE>
-gdn_status launch_verify_stream_dims(const VerifyArgs &a, const PrevCommit &c, cudaStream_t s) {
+gdn_status launch_verify_stream_dims(const VerifyArgs &a, const PrevCommit &c, const Serving &L, cudaStream_t s) {
   switch (a.dk * 1000 + a.dv) {
-    case 32064: return launch_verify_stream_n<32, 64, FUSE>(a, c, s);
-    case 32128: return launch_verify_stream_n<32, 128, FUSE>(a, c, s);
-    case 64064: return launch_verify_stream_n<64, 64, FUSE>(a, c, s);
-    case 64128: return launch_verify_stream_n<64, 128, FUSE>(a, c, s);
-    case 128064: return launch_verify_stream_n<128, 64, FUSE>(a, c, s);
-    default: return launch_verify_stream_n<128, 128, FUSE>(a, c, s);
+    case 32064: return launch_verify_stream_n<32, 64, FUSE>(a, c, L, s);
+    case 32128: return launch_verify_stream_n<32, 128, FUSE>(a, c, L, s);
+    case 64064: return launch_verify_stream_n<64, 64, FUSE>(a, c, L, s);
+    case 64128: return launch_verify_stream_n<64, 128, FUSE>(a, c, L, s);
+    case 128064: return launch_verify_stream_n<128, 64, FUSE>(a, c, L, s);
+    default: return launch_verify_stream_n<128, 128, FUSE>(a, c, L, s);
   }
 }
 
-template <int DK, int DV>
-gdn_status launch_commit(const CommitArgs &a, cudaStream_t stream) {
+template <int DK, int DV, bool SV>
+gdn_status launch_commit_sv(const CommitArgs &a, const Serving &L, cudaStream_t stream) {
   const size_t smem = commit_smem_bytes(a.max_path, DK, DV);
-  if (cudaFuncSetAttribute(commit_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+  if (cudaFuncSetAttribute(commit_kernel<DK, DV, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
       cudaSuccess)
     return GDN_ECUDA;
   const long long blocks = (long long)a.B * a.H;
-  commit_kernel<DK, DV><<<unsigned(blocks), kThreads, smem, stream>>>(a);
+  commit_kernel<DK, DV, SV><<<unsigned(blocks), kThreads, smem, stream>>>(a, L);
   return launch_status();
+}
+
+template <int DK, int DV>
+gdn_status launch_commit(const CommitArgs &a, const Serving &L, cudaStream_t stream) {
+  return is_plain(L) ? launch_commit_sv<DK, DV, false>(a, L, stream) : launch_commit_sv<DK, DV, true>(a, L, stream);
 }
 
 template <int DK>
@@ -210,11 +267,102 @@ gdn_status launch_storeall(const StoreallArgs &a, cudaStream_t stream) {
   return launch_status();
 }
 
+gdn_status verify_simt_impl(const float *ST, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *beta, const float *g, const int32_t *parent, const int32_t *cu_nodes,
+                            int32_t B, int32_t H, int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes,
+                            const Serving &L, float *o, float *U, float *G, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
+                                    max_nodes, o, U, G, status, L);
+  if (st != GDN_OK || B == 0 || T == 0) return st;
+  if ((st = check_device()) != GDN_OK) return st;
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d_k) {
+    case 32: return launch_verify_simt<32>(a, L, s);
+    case 64: return launch_verify_simt<64>(a, L, s);
+    default: return launch_verify_simt<128>(a, L, s);
+  }
+}
+
+gdn_status verify_impl(const float *ST, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *beta,
+                       const float *g, const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H,
+                       int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes, const Serving &L, float *o, float *U,
+                       float *G, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
+                                    max_nodes, o, U, G, status, L);
+  if (st != GDN_OK || B == 0 || T == 0) return st;
+  if (d_v == 32 || (d_k == 32 && max_nodes > kStreamMaxNodes))
+    return verify_simt_impl(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, L, o, U, G,
+                            status, stream);
+  if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (max_nodes <= kStreamMaxNodes)  // small trees: CUDA-core streaming kernel
+    return launch_verify_stream_dims<false>(a, PrevCommit{}, L, s);
+  if (d_k == 128) return d_v == 128 ? launch_verify_tc<128, 128>(a, L, s) : launch_verify_tc<128, 64>(a, L, s);
+  return d_v == 128 ? launch_verify_tc<64, 128>(a, L, s) : launch_verify_tc<64, 64>(a, L, s);
+}
+
+gdn_status commit_impl(float *ST, const float *U, const float *G, const uint16_t *k, const int32_t *parent,
+                       const int32_t *cu_nodes, const int32_t *path, const int32_t *path_len, int32_t B, int32_t H,
+                       int32_t T, int32_t d_k, int32_t d_v, int32_t max_path, const Serving &L, int32_t *status,
+                       gdn_stream_t stream) {
+  gdn_status st = check_commit_args(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v,
+                                    max_path, status);
+  if (st != GDN_OK || B == 0) return st;
+  if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (d_k * 1000 + d_v) {
+    case 32032: return launch_commit<32, 32>(a, L, s);
+    case 32064: return launch_commit<32, 64>(a, L, s);
+    case 32128: return launch_commit<32, 128>(a, L, s);
+    case 64032: return launch_commit<64, 32>(a, L, s);
+    case 64064: return launch_commit<64, 64>(a, L, s);
+    case 64128: return launch_commit<64, 128>(a, L, s);
+    case 128032: return launch_commit<128, 32>(a, L, s);
+    case 128064: return launch_commit<128, 64>(a, L, s);
+    default: return launch_commit<128, 128>(a, L, s);
+  }
+}
+
+gdn_status commit_verify_impl(float *ST, const float *U_prev, const float *G_prev, const uint16_t *k_prev,
+                              const int32_t *parent_prev, const int32_t *cu_nodes_prev, const int32_t *path,
+                              const int32_t *path_len, int32_t T_prev, int32_t max_path, const uint16_t *q,
+                              const uint16_t *k, const uint16_t *v, const float *beta, const float *g,
+                              const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
+                              int32_t d_k, int32_t d_v, int32_t max_nodes, const Serving &L, float *o, float *U,
+                              float *G, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_commit_args(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H,
+                                    T_prev, d_k, d_v, max_path, status);
+  if (st != GDN_OK) return st;
+  if ((st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G,
+                              status, L)) != GDN_OK)
+    return st;
+  if (B == 0) return GDN_OK;
+  if (U && U == U_prev) return GDN_EINVAL;  // this step's pseudo-values may not overwrite the previous ones
+  const bool fusable = T > 0 && d_v != 32 && max_nodes <= kStreamMaxNodes && max_path <= kFuseMaxPath;
+  if (!fusable) {  // the same result from the two kernels in order
+    if ((st = commit_impl(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H, T_prev, d_k,
+                          d_v, max_path, L, status, stream)) != GDN_OK)
+      return st;
+    return verify_impl(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, L, o, U, G, status,
+                       stream);
+  }
+  if ((st = check_device()) != GDN_OK) return st;
+  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
+  PrevCommit c{ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path};
+  return launch_verify_stream_dims<true>(a, c, L, reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return 2; }
+int32_t gdn_abi_version(void) { return 3; }
 
 const char *gdn_status_str(gdn_status s) {
   switch (s) {
@@ -234,17 +382,8 @@ gdn_status gdn_tree_verify_simt(const float *ST, const uint16_t *q, const uint16
                                 int32_t H, int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes,
                                 float *o, float *U, float *G, int32_t *status,
                                 gdn_stream_t stream) {
-  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
-                                    max_nodes, o, U, G, status);
-  if (st != GDN_OK || B == 0 || T == 0) return st;
-  if ((st = check_device()) != GDN_OK) return st;
-  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (d_k) {
-    case 32: return launch_verify_simt<32>(a, s);
-    case 64: return launch_verify_simt<64>(a, s);
-    default: return launch_verify_simt<128>(a, s);
-  }
+  return verify_simt_impl(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, Serving{}, o, U, G,
+                          status, stream);
 }
 
 gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -252,44 +391,38 @@ gdn_status gdn_tree_verify(const float *ST, const uint16_t *q, const uint16_t *k
                            const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T, int32_t d_k,
                            int32_t d_v, int32_t max_nodes, float *o, float *U, float *G,
                            int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v,
-                                    max_nodes, o, U, G, status);
-  if (st != GDN_OK || B == 0 || T == 0) return st;
-  if (d_v == 32 || (d_k == 32 && max_nodes > kStreamMaxNodes))
-    return gdn_tree_verify_simt(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o,
-                                U, G, status, stream);
-  if ((st = check_device()) != GDN_OK) return st;
-  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
-  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (max_nodes <= kStreamMaxNodes)  // small trees: CUDA-core streaming kernel
-    return launch_verify_stream_dims<false>(a, PrevCommit{}, s);
-  if (d_k == 128) return d_v == 128 ? launch_verify_tc<128, 128>(a, s) : launch_verify_tc<128, 64>(a, s);
-  return d_v == 128 ? launch_verify_tc<64, 128>(a, s) : launch_verify_tc<64, 64>(a, s);
+  return verify_impl(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, Serving{}, o, U, G, status,
+                     stream);
+}
+
+gdn_status gdn_tree_verify_ex(const float *ST, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const float *beta, const float *g, const int32_t *parent,
+                              const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T, int32_t d_k,
+                              int32_t d_v, int32_t max_nodes, const gdn_layout *layout, float *o,
+                              float *U, float *G, int32_t *status, gdn_stream_t stream) {
+  Serving L;
+  const gdn_status st = make_serving(layout, H, true, L);
+  if (st != GDN_OK) return st;
+  return verify_impl(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, L, o, U, G, status, stream);
 }
 
 gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint16_t *k,
                            const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
                            const int32_t *path_len, int32_t B, int32_t H, int32_t T, int32_t d_k,
                            int32_t d_v, int32_t max_path, int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_commit_args(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v,
-                                    max_path, status);
-  if (st != GDN_OK || B == 0) return st;
-  if ((st = check_device()) != GDN_OK) return st;
-  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
-  CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  switch (d_k * 1000 + d_v) {
-    case 32032: return launch_commit<32, 32>(a, s);
-    case 32064: return launch_commit<32, 64>(a, s);
-    case 32128: return launch_commit<32, 128>(a, s);
-    case 64032: return launch_commit<64, 32>(a, s);
-    case 64064: return launch_commit<64, 64>(a, s);
-    case 64128: return launch_commit<64, 128>(a, s);
-    case 128032: return launch_commit<128, 32>(a, s);
-    case 128064: return launch_commit<128, 64>(a, s);
-    default: return launch_commit<128, 128>(a, s);
-  }
+  return commit_impl(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, Serving{}, status,
+                     stream);
+}
+
+gdn_status gdn_tree_commit_ex(float *ST, const float *U, const float *G, const uint16_t *k,
+                              const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
+                              const int32_t *path_len, int32_t B, int32_t H, int32_t T, int32_t d_k,
+                              int32_t d_v, int32_t max_path, const gdn_layout *layout, int32_t *status,
+                              gdn_stream_t stream) {
+  Serving L;
+  const gdn_status st = make_serving(layout, H, false, L);
+  if (st != GDN_OK) return st;
+  return commit_impl(ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, L, status, stream);
 }
 
 gdn_status gdn_tree_accept_greedy(const int32_t *draft_tok, const int32_t *target_tok,
@@ -321,27 +454,26 @@ gdn_status gdn_tree_commit_verify(float *ST, const float *U_prev, const float *G
                                   const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
                                   int32_t d_k, int32_t d_v, int32_t max_nodes, float *o, float *U,
                                   float *G, int32_t *status, gdn_stream_t stream) {
-  gdn_status st = check_commit_args(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H,
-                                    T_prev, d_k, d_v, max_path, status);
+  return commit_verify_impl(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path,
+                            q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, Serving{}, o, U, G,
+                            status, stream);
+}
+
+gdn_status gdn_tree_commit_verify_ex(float *ST, const float *U_prev, const float *G_prev,
+                                     const uint16_t *k_prev, const int32_t *parent_prev,
+                                     const int32_t *cu_nodes_prev, const int32_t *path,
+                                     const int32_t *path_len, int32_t T_prev, int32_t max_path,
+                                     const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const float *beta, const float *g, const int32_t *parent,
+                                     const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
+                                     int32_t d_k, int32_t d_v, int32_t max_nodes, const gdn_layout *layout,
+                                     float *o, float *U, float *G, int32_t *status, gdn_stream_t stream) {
+  Serving L;
+  const gdn_status st = make_serving(layout, H, true, L);
   if (st != GDN_OK) return st;
-  if ((st = check_verify_args(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G,
-                              status)) != GDN_OK)
-    return st;
-  if (B == 0) return GDN_OK;
-  if (U && U == U_prev) return GDN_EINVAL;  // this step's pseudo-values may not overwrite the previous ones
-  const bool fusable = T > 0 && d_v != 32 && max_nodes <= kStreamMaxNodes && max_path <= kFuseMaxPath;
-  if (!fusable) {  // the same result from the two kernels in order
-    if ((st = gdn_tree_commit(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, B, H, T_prev,
-                              d_k, d_v, max_path, status, stream)) != GDN_OK)
-      return st;
-    return gdn_tree_verify(ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status,
-                           stream);
-  }
-  if ((st = check_device()) != GDN_OK) return st;
-  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
-  VerifyArgs a{ST, q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, o, U, G, status};
-  PrevCommit c{ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path};
-  return launch_verify_stream_dims<true>(a, c, reinterpret_cast<cudaStream_t>(stream));
+  return commit_verify_impl(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_prev, path, path_len, T_prev, max_path,
+                            q, k, v, beta, g, parent, cu_nodes, B, H, T, d_k, d_v, max_nodes, L, o, U, G, status,
+                            stream);
 }
 
 gdn_status gdn_tree_verify_storeall(const float *ST, const uint16_t *q, const uint16_t *k,

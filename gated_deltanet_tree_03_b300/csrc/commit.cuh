@@ -35,8 +35,8 @@ __host__ __device__ inline size_t commit_smem_bytes(int max_path, int dk, int dv
          + size_t(max_path) * (dk + dv) * 4;       // exp(G_l - G_j) k_j and u_j per path entry
 }
 
-template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
+template <int DK, int DV, bool SV>
+__global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving sv) {
   constexpr int DV4 = DV / 4;
   constexpr int J = DK * DV4 / kThreads;  // float4 of the state per thread
   constexpr int ROWSTEP = kThreads / DV4;  // state rows between a thread's float4s
@@ -54,7 +54,13 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
   const int tid = threadIdx.x;
   const int pair = blockIdx.x;
   const int h = pair % a.H, r = pair / a.H;
-  float *ST = a.ST + size_t(pair) * DK * DV;
+  const int si = state_of<SV>(sv, r);  // the request's state (pool slot)
+  if (si < 0) {  // padding request, or a slot outside the pool: the state is not touched
+    if (si == kBadSlot && tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
+  float *ST = a.ST + (SV ? size_t(si) * a.H + h : size_t(pair)) * DK * DV;
+  const int HK = a.H / qk_group<SV>(sv), hk = h / qk_group<SV>(sv);  // q/k heads, this value head's q/k head
 
   if (tid == 0) {
     const int L = a.path_len[r];
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a) {
     for (int i = tid; i < L * DK; i += kThreads) {
       const int s = i / DK, row = i % DK;
       const size_t th = size_t(t0 + path_r[s]) * a.H + h;
-      kw[i] = expf(Gl - a.G[th]) * bf16_to_f32(a.k[th * DK + row]);
+      kw[i] = expf(Gl - a.G[th]) * bf16_to_f32(a.k[(size_t(t0 + path_r[s]) * HK + hk) * DK + row]);
     }
     for (int i = tid; i < L * DV4; i += kThreads) {
       const int s = i / DV4, c4 = i % DV4;

@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads) verify_storeall_kernel(StoreallArgs 
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
     return;
   }
-  if (!analyse_tree(ts, a.parent, a.g, a.beta, t0, n, h, a.H)) {
+  if (!analyse_tree<false>(ts, a.parent, a.g, a.beta, t0, n, h, a.H, Serving{})) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
     return;
   }

@@ -34,8 +34,8 @@ __host__ __device__ inline size_t verify_simt_smem_bytes(int M, int DK) {
                           + size_t(M) * M * 2); // A, P
 }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
+template <int DK, bool SV>
+__global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a, Serving sv) {
   __shared__ TreeSmem ts;
   extern __shared__ __align__(16) float dyn[];
   const int tile = blockIdx.x, h = blockIdx.y, r = blockIdx.z;
@@ -43,6 +43,11 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
   const int M = a.max_nodes;
+  const int si = state_of<SV>(sv, r);
+  if (si < 0) {
+    if (si == kBadSlot && tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
   if (!offsets_ok(t0, n, a.T)) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
     return;
@@ -52,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_TOO_MANY_NODES);
     return;
   }
-  if (!analyse_tree(ts, a.parent, a.g, a.beta, t0, n, h, a.H)) {
+  if (!analyse_tree<SV>(ts, a.parent, a.g, a.beta, t0, n, h, a.H, sv)) {
     if (tid == 0 && tile == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
     return;
   }
@@ -66,14 +71,15 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
   float *Pc = Ac + M * M;
 
   const int H = a.H, dv = a.dv, c0 = tile * 32;
+  const int HK = H / qk_group<SV>(sv), hk = h / qk_group<SV>(sv);  // q/k heads, this value head's q/k head
   // stage the node block and the state slice
   for (int i = tid; i < 2 * n * DK; i += kThreads) {
     const int row = i / DK, col = i % DK;
     const int t = row < n ? row : row - n;
     const uint16_t *src = row < n ? a.k : a.q;
-    Xs[(row < n ? row : M + t) * DK + col] = bf16_to_f32(src[(size_t(t0 + t) * H + h) * DK + col]);
+    Xs[(row < n ? row : M + t) * DK + col] = bf16_to_f32(src[(size_t(t0 + t) * HK + hk) * DK + col]);
   }
-  const float *ST = a.ST + (size_t(r) * H + h) * DK * dv + c0;
+  const float *ST = a.ST + (size_t(si) * H + h) * DK * dv + c0;
   for (int i = tid; i < DK * 32; i += kThreads) STs[i] = ST[size_t(i >> 5) * dv + (i & 31)];
   for (int i = tid; i < n * 32; i += kThreads)
     Vs[i] = bf16_to_f32(a.v[(size_t(t0 + (i >> 5)) * H + h) * dv + c0 + (i & 31)]);
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) verify_simt_kernel(VerifyArgs a) {
       out = fmaf(Pc[t * M + j], Us[j * 32 + c], out);
     }
     const size_t row = (size_t(t0 + t) * H + h) * dv + c0 + c;
-    a.o[row] = out;
+    a.o[row] = query_scale<SV>(sv) * out;  // o is linear in q
     a.U[row] = Us[i];
     if (tile == 0 && c == 0) a.G[size_t(t0 + t) * H + h] = ts.G[t];
   }

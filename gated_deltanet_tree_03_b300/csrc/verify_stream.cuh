@@ -54,9 +54,9 @@ struct PrevCommit {
 // State rows each thread keeps in flight (more rows cost resident CTAs; 16 measured best).
 __host__ __device__ constexpr int stream_prefetch_rows(int) { return 16; }
 
-template <int DK, int DV, int NMAX, bool FUSE>
+template <int DK, int DV, int NMAX, bool FUSE, bool SV>
 __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE))
-    verify_stream_kernel(VerifyArgs a, PrevCommit c) {
+    verify_stream_kernel(VerifyArgs a, PrevCommit c, Serving sv) {
   constexpr int NT = DV / 2;    // threads
   constexpr int NW = NT / 32;   // warps
   constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
@@ -74,7 +74,13 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int pair = blockIdx.x, h = pair % a.H, r = pair / a.H;
   const int col2 = tid;  // this thread's float2 column index within a state row
-  const float2 *st = reinterpret_cast<const float2 *>(a.ST + size_t(pair) * DK * DV) + col2;
+  const int si = state_of<SV>(sv, r);  // the request's state (pool slot)
+  if (si < 0) {  // padding request, or a slot outside the pool: nothing is read or written
+    if (si == kBadSlot && tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_SLOT);
+    return;
+  }
+  const size_t st_off = (SV ? size_t(si) * a.H + h : size_t(pair)) * DK * DV;
+  const float2 *st = reinterpret_cast<const float2 *>(a.ST + st_off) + col2;
 
   // 1) the first state rows go out before any dependent load
   float2 s[kStreamPF];
@@ -95,6 +101,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     vok = false;
   }
   const int H = a.H;
+  const int HK = H / qk_group<SV>(sv), hk = h / qk_group<SV>(sv);  // q/k heads, this value head's q/k head
 
   // 2b) fused: the previous step's accepted path (same checks and effect as gdn_tree_commit)
   int Lc = 0;
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
       for (int i = tid; i < L * DK; i += NT) {
         const int q = i / DK, row = i % DK;
         const size_t th = size_t(tp0 + path_r[q]) * H + h;
-        Ws[q][row] = expf(Gl - c.G[th]) * bf16_to_f32(c.k[th * DK + row]);
+        Ws[q][row] = expf(Gl - c.G[th]) * bf16_to_f32(c.k[(size_t(tp0 + path_r[q]) * HK + hk) * DK + row]);
       }
 #pragma unroll
       for (int q = 0; q < LW; ++q)
@@ -142,7 +149,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     const int t = row < NMAX ? row : row - NMAX;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (t < n) {
-      const uint16_t *src = (row < NMAX ? a.k : a.q) + (size_t(t0 + t) * H + h) * DK + 4 * c4;
+      const uint16_t *src = (row < NMAX ? a.k : a.q) + (size_t(t0 + t) * HK + hk) * DK + 4 * c4;
       const uint2 w = *reinterpret_cast<const uint2 *>(src);
       const float2 lo = bf16x2_to_f32(w.x), hi = bf16x2_to_f32(w.y);
       x = make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -158,8 +165,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     const int p = a.parent[t0 + tid];
     bad = (p < -1 || p >= tid);
     par_s[tid] = p;
-    g_s[tid] = a.g[size_t(t0 + tid) * H + h];
-    beta_s[tid] = a.beta[size_t(t0 + tid) * H + h];
+    gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tid) * H + h, h, g_s[tid], beta_s[tid]);
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     for (int g4 = 0; g4 < kStreamPF; g4 += 4) {
       if constexpr (FUSE) {
         if (Lc > 0) {  // fold the accepted path into these four rows and write them back once
-          float2 *stw = reinterpret_cast<float2 *>(c.ST + size_t(pair) * DK * DV) + col2;
+          float2 *stw = reinterpret_cast<float2 *>(c.ST + st_off) + col2;
 #pragma unroll
           for (int i = 0; i < 4; ++i) s[g4 + i] = make_float2(decay * s[g4 + i].x, decay * s[g4 + i].y);
 #pragma unroll
@@ -307,7 +313,8 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
         }
       }
       const size_t row = (size_t(t0 + t) * H + h) * DV2 + col2;
-      __stcs(reinterpret_cast<float2 *>(a.o) + row, o);
+      const float qsc = query_scale<SV>(sv);  // o is linear in q
+      __stcs(reinterpret_cast<float2 *>(a.o) + row, make_float2(qsc * o.x, qsc * o.y));
       __stcs(reinterpret_cast<float2 *>(a.U) + row, u[t]);
     }
   }

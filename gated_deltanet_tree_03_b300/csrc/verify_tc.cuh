@@ -131,12 +131,21 @@ struct TcShared {
   int split_ok, epi_ok[3];
 };
 
-// Nodes of pair p; false for a pair that is skipped (empty, too many nodes, bad offsets).
-__device__ __forceinline__ bool tc_pair_nodes(const VerifyArgs &a, int p, int &t0, int &n) {
+// Nodes and state slot of pair p; false for a pair that is skipped (padding request, slot
+// outside the pool, empty, too many nodes, bad offsets).
+template <bool SV>
+__device__ __forceinline__ bool tc_pair_nodes(const VerifyArgs &a, const Serving &sv, int p, int &t0, int &n,
+                                              int &si) {
   const int r = p / a.H;
   t0 = a.cu_nodes[r];
   n = a.cu_nodes[r + 1] - t0;
-  return offsets_ok(t0, n, a.T) && n > 0 && n <= a.max_nodes;
+  if constexpr (SV) {
+    si = state_of<SV>(sv, r);
+    return si >= 0 && offsets_ok(t0, n, a.T) && n > 0 && n <= a.max_nodes;
+  } else {
+    si = r;
+    return offsets_ok(t0, n, a.T) && n > 0 && n <= a.max_nodes;
+  }
 }
 
 // Bounded wait that also gives up when another role has raised the abort flag.
@@ -163,10 +172,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool SV>
 __global__ void __launch_bounds__(kTcThreads, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_v, VerifyArgs a, TcLayout lay) {
+                     const __grid_constant__ CUtensorMap tm_v, VerifyArgs a, TcLayout lay, Serving sv) {
   static_assert(DK == 64 || DK == 128, "tensor-core verify needs d_k in {64, 128}");
   static_assert(DV == 64 || DV == 128, "tensor-core verify needs d_v in {64, 128}");
   constexpr int NCHUNK = DK / kChunkRows;              // ring slots per pair
@@ -222,9 +231,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       uint32_t u = 0;
       for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-        int t0, n;
-        if (!tc_pair_nodes(a, p, t0, n)) continue;
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(a.ST + size_t(p) * DK * DV);
+        int t0, n, si;
+        if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
+        const size_t st_idx = SV ? size_t(si) * a.H + p % a.H : size_t(p);
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(a.ST + st_idx * DK * DV);
         bool ok = true;
         for (int c = 0; c < NCHUNK; ++c, ++u) {
           const int s = int(u % uint32_t(R));
@@ -248,9 +258,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint8_t *X = base + lay.x;
       uint32_t i = 0;
       for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-        int t0, n;
-        if (!tc_pair_nodes(a, p, t0, n)) continue;
-        const int h = p % a.H, b = int(i & 1u);
+        int t0, n, si;
+        if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
+        const int h = p % a.H, b = int(i & 1u), hk = h / qk_group<SV>(sv);
         // the X buffer is free once the MMAs of pair i-1 are done, the v buffer once the
         // epilogue of pair i-1 has formed its R (neither barrier can complete again before
         // this copy is issued, so the parity cannot have moved on); X goes first so the MMAs
@@ -259,8 +269,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::mbar_arrive_expect_tx(&sh.node_full[b], x_bytes);
 #pragma unroll
         for (int c = 0; c < NCHUNK; ++c) {
-          ptx::tma_load_3d(X + c * kRegionBytes, &tm_k, &sh.node_full[b], c * 64, h, t0);
-          ptx::tma_load_3d(X + c * kRegionBytes + Np * 128, &tm_q, &sh.node_full[b], c * 64, h, t0);
+          ptx::tma_load_3d(X + c * kRegionBytes, &tm_k, &sh.node_full[b], c * 64, hk, t0);
+          ptx::tma_load_3d(X + c * kRegionBytes + Np * 128, &tm_q, &sh.node_full[b], c * 64, hk, t0);
         }
         issued = ++i;
         if (i > 1 && !tc_wait(&sh.v_empty, (i - 2) & 1u, sh, a.status)) break;
@@ -276,8 +286,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t id_gram = ptx::idesc_bf16_f32(128, Np);
       uint32_t u = 0, i = 0;
       for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-        int t0, n;
-        if (!tc_pair_nodes(a, p, t0, n)) continue;
+        int t0, n, si;
+        if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
         const int b = int(i & 1u);
         const uint32_t ph = (i >> 1) & 1u;
         if (!tc_wait(&sh.tmem_empty[b], ph ^ 1u, sh, a.status)) break;
@@ -317,11 +327,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ tree analysis
     uint32_t i = 0;
     for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-      int t0, n;
+      int t0, n, si;
       const int h = p % a.H;
-      if (!tc_pair_nodes(a, p, t0, n)) {
+      if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) {
         if (lane == 0 && h == 0) {
-          if (!offsets_ok(t0, n, a.T)) report(a.status, GDN_STATUS_BAD_OFFSETS);
+          if (SV && si < 0) {
+            if (si == kBadSlot) report(a.status, GDN_STATUS_BAD_SLOT);
+          } else if (!offsets_ok(t0, n, a.T)) report(a.status, GDN_STATUS_BAD_OFFSETS);
           else if (n > a.max_nodes) report(a.status, GDN_STATUS_TOO_MANY_NODES);
         }
         continue;
@@ -340,8 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int pr = a.parent[t0 + t];
           bad |= (pr < -1 || pr >= t);
           ts.par[t] = pr;
-          ts.g[t] = a.g[size_t(t0 + t) * a.H + h];
-          ts.beta[t] = a.beta[size_t(t0 + t) * a.H + h];
+          gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + t) * a.H + h, h, ts.g[t], ts.beta[t]);
         }
       }
       bad = __any_sync(0xffffffffu, bad);
@@ -433,8 +444,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t id_uo = ptx::idesc_bf16_f32(128, 2 * Np);
     uint32_t i = 0;
     for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-      int t0, n;
-      if (!tc_pair_nodes(a, p, t0, n)) continue;
+      int t0, n, si;
+      if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
       const int h = p % a.H, b = int(i & 1u);
       const uint32_t ph = (i >> 1) & 1u;
       // tree ready (the barrier also ends every epilogue thread's use of the previous pair).
@@ -624,7 +635,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int t = c0 + jj;
             if (t < n) {
               const size_t o_row = (size_t(t0 + t) * a.H + h) * DV + v;
-              __stcs(a.o + o_row, fmaf(ts.gam[t], qs[jj], ww[jj]));
+              const float ov = fmaf(ts.gam[t], qs[jj], ww[jj]);
+              __stcs(a.o + o_row, SV ? query_scale<SV>(sv) * ov : ov);  // o is linear in q
               __stcs(a.U + o_row, uu[jj]);
             }
           }
@@ -647,8 +659,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int KCSTEP = kSplitThreads / DV;
     uint32_t u = 0;
     for (int p = blockIdx.x; p < npairs; p += gridDim.x) {
-      int t0, n;
-      if (!tc_pair_nodes(a, p, t0, n)) continue;
+      int t0, n, si;
+      if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
       bool ok = true;
       for (int c = 0; c < NCHUNK; ++c, ++u) {
         const int s = int(u % uint32_t(R));

@@ -364,6 +364,55 @@ def make_random_batch(seed: int, B: int, H: int, d: int, n_range=(1, 16), fanout
     return build_batch(rng, parents, paths, H=H, dk=d, dv=d, gate=gate, name=f"random_seed{seed}")
 
 
+@dataclass
+class ServingInputs:
+    """Serving-layout inputs that go with a TreeBatch (see ``make_serving_batch``)."""
+
+    pool: np.ndarray  # [n_slots, H, dk, dv] fp32 state pool
+    slot: np.ndarray  # [B] int32 state slot per request, -1 = padding request
+    H_qk: int  # query/key heads (H is a multiple)
+    q: np.ndarray  # [T, H_qk, dk] uint16 (bf16 bits)
+    k: np.ndarray  # [T, H_qk, dk] uint16
+    q_scale: float
+    a_raw: np.ndarray  # [T, H] fp32 gate pre-activation
+    b_raw: np.ndarray  # [T, H] fp32 write-strength pre-activation
+    A_log: np.ndarray  # [H] fp32
+    dt_bias: np.ndarray  # [H] fp32
+
+    @property
+    def gates(self):
+        return self.a_raw, self.b_raw, self.A_log, self.dt_bias
+
+
+def make_serving_batch(seed: int, B: int, H: int, H_qk: int, d: int, n_range=(1, 16), n_slots: int | None = None,
+                       pad_every: int = 0, q_scale: float | None = None, **tree_kw):
+    """A random ragged batch laid out as a serving engine holds it: states in a pool larger than
+    the batch (distinct random slots, every ``pad_every``-th request a -1 padding slot), q and k
+    with H_qk heads, a query scale (default d^-1/2), and gate pre-activations
+    a_raw ~ N(0, 1), b_raw ~ N(0, 1), A_log = ln U(1, 16), dt_bias ~ U(-7, -2) (per-step decays
+    of roughly 0.8 .. 1 once mapped through the gate). Returns (TreeBatch, ServingInputs); the
+    TreeBatch's own q, k and ST0 are not used by the serving layout."""
+    tb = make_random_batch(seed=seed, B=B, H=H, d=d, n_range=n_range, **tree_kw)
+    rng = np.random.default_rng([seed, 0x5e])
+    n_slots = n_slots if n_slots is not None else 2 * B + 3
+    if n_slots < B:
+        raise ValueError("the pool must hold a state per request")
+    slot = rng.permutation(n_slots)[:B].astype(np.int32)
+    if pad_every:
+        slot[pad_every - 1::pad_every] = -1
+    pool = (rng.standard_normal((n_slots, H, d, d), dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    T = tb.T
+    sv = ServingInputs(
+        pool=pool, slot=slot, H_qk=H_qk,
+        q=_normalised_bf16(rng, (T, H_qk, d)), k=_normalised_bf16(rng, (T, H_qk, d)),
+        q_scale=float(d ** -0.5) if q_scale is None else float(q_scale),
+        a_raw=rng.standard_normal((T, H), dtype=np.float32),
+        b_raw=rng.standard_normal((T, H), dtype=np.float32),
+        A_log=np.log(rng.uniform(1.0, 16.0, size=H)).astype(np.float32),
+        dt_bias=rng.uniform(-7.0, -2.0, size=H).astype(np.float32))
+    return tb, sv
+
+
 def draw_tokens(rng: np.random.Generator, parent: np.ndarray, cu_nodes: np.ndarray, vocab: int = 50,
                 p_match: float = 0.7):
     """Synthetic draft / target tokens for greedy acceptance tests.

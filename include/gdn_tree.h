@@ -75,6 +75,41 @@ typedef enum gdn_status {
 #define GDN_STATUS_TIMEOUT 8u        /* a bounded wait on an asynchronous copy gave up       */
 #define GDN_STATUS_BAD_OFFSETS 16u   /* cu_nodes not non-decreasing inside [0, T]            */
 #define GDN_STATUS_PATH_TRUNCATED 32u /* an accepted path was longer than max_path            */
+#define GDN_STATUS_BAD_SLOT 64u      /* a state slot outside [0, n_slots) and not -1         */
+
+/*
+ * gdn_layout - serving layout of the *_ex entry points: how an inference engine that hosts
+ * the layer (the TreeWY page evaluates it inside vLLM, experiments section) lays out its
+ * recurrent states and heads. A NULL layout, or a zero-initialised one, is the plain layout
+ * of gdn_tree_verify / gdn_tree_commit.
+ *
+ *  state_slot [B] int32 (device, or NULL): request r's state is ST[state_slot[r]] in a pool
+ *             ST[n_slots][H][d_k][d_v]; -1 marks a padding request, which is skipped (no
+ *             outputs, no state change); any other value outside [0, n_slots) sets
+ *             GDN_STATUS_BAD_SLOT and skips the request. NULL: request r owns ST[r].
+ *             Requests committed in one call must name distinct slots (verify may share).
+ *  n_slots    states in the pool (> 0 when state_slot is non-NULL; ignored otherwise).
+ *  H_qk       heads of q and k (0 = H). H must be a multiple of H_qk; value head h reads
+ *             q/k head h / (H / H_qk) (grouped heads: consecutive value heads share a key).
+ *             q and k are then [T][H_qk][d_k]; v, beta, g, o, U, G and ST keep H heads.
+ *  q_scale    every query is multiplied by q_scale (o = S (q_scale q)); 0 or 1 = unscaled.
+ *  a_raw, b_raw [T][H] fp32, A_log, dt_bias [H] fp32 (device; all four or none): gate fusion.
+ *             With them the kernels form each node's gate and write strength themselves,
+ *                 g = -exp(A_log[h]) * softplus(a_raw + dt_bias[h]),  b = sigmoid(b_raw),
+ *             softplus(x) = ln(1 + e^x), sigmoid(x) = 1 / (1 + e^-x) (the gated delta rule's
+ *             decay and write strength in the Gated DeltaNet parametrisation), and the beta
+ *             and g arguments are not read (they may be NULL).
+ */
+typedef struct gdn_layout {
+    const int32_t *state_slot;
+    int32_t n_slots;
+    int32_t H_qk;
+    float q_scale;
+    const float *a_raw;
+    const float *b_raw;
+    const float *A_log;
+    const float *dt_bias;
+} gdn_layout;
 
 /*
  * gdn_tree_verify - outputs and pseudo-values of every draft node (tree-structured WY form).
@@ -150,7 +185,7 @@ gdn_status gdn_tree_commit(float *ST, const float *U, const float *G, const uint
  *   cu_nodes, B, H, T, d_k, d_v, max_nodes
  *   o, U, G                          out     this step's outputs; U must not alias U_prev
  *   status                           out     optional, bits of both operations
- * One fused kernel runs when d_v is 64 or 128, max_nodes <= 8 and max_path <= 8; otherwise the
+ * One fused kernel runs when d_v is 64 or 128, max_nodes <= 8 and max_path <= 4; otherwise the
  * two kernels run in order on `stream`, with the same result.
  */
 gdn_status gdn_tree_commit_verify(float *ST, const float *U_prev, const float *G_prev,
@@ -213,6 +248,43 @@ gdn_status gdn_tree_accept_greedy(const int32_t *draft_tok, const int32_t *targe
                                   const int32_t *parent, const int32_t *cu_nodes, int32_t B,
                                   int32_t T, int32_t max_nodes, int32_t max_path, int32_t *path,
                                   int32_t *path_len, int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_verify_ex, gdn_tree_commit_ex, gdn_tree_commit_verify_ex - the entry points above
+ * under a serving layout (gdn_layout, a HOST pointer to a struct of device pointers; NULL =
+ * plain layout). Arguments, results and errors are otherwise those of gdn_tree_verify,
+ * gdn_tree_commit and gdn_tree_commit_verify, with ST the state pool when state_slot is set.
+ * Commit reads state_slot, n_slots and H_qk (for k) and ignores the rest. The layout fields
+ * are checked on the host: H_qk < 0 or not dividing H, a non-finite q_scale, state_slot
+ * without n_slots > 0, or some but not all four gate arrays give GDN_EINVAL; a misaligned
+ * array gives GDN_EALIGN.
+ */
+gdn_status gdn_tree_verify_ex(const float *ST, const uint16_t *q, const uint16_t *k,
+                              const uint16_t *v, const float *beta, const float *g,
+                              const int32_t *parent, const int32_t *cu_nodes, int32_t B,
+                              int32_t H, int32_t T, int32_t d_k, int32_t d_v, int32_t max_nodes,
+                              const gdn_layout *layout, float *o, float *U, float *G,
+                              int32_t *status, gdn_stream_t stream);
+
+gdn_status gdn_tree_commit_ex(float *ST, const float *U, const float *G, const uint16_t *k,
+                              const int32_t *parent, const int32_t *cu_nodes, const int32_t *path,
+                              const int32_t *path_len, int32_t B, int32_t H, int32_t T,
+                              int32_t d_k, int32_t d_v, int32_t max_path, const gdn_layout *layout,
+                              int32_t *status, gdn_stream_t stream);
+
+/* The previous step's requests and this step's are the same requests in the same order; both
+ * use layout->state_slot, and k_prev has H_qk heads like k. q_scale and the gate arrays belong
+ * to this step's tree (the previous step's gates are already folded into G_prev). */
+gdn_status gdn_tree_commit_verify_ex(float *ST, const float *U_prev, const float *G_prev,
+                                     const uint16_t *k_prev, const int32_t *parent_prev,
+                                     const int32_t *cu_nodes_prev, const int32_t *path,
+                                     const int32_t *path_len, int32_t T_prev, int32_t max_path,
+                                     const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const float *beta, const float *g, const int32_t *parent,
+                                     const int32_t *cu_nodes, int32_t B, int32_t H, int32_t T,
+                                     int32_t d_k, int32_t d_v, int32_t max_nodes,
+                                     const gdn_layout *layout, float *o, float *U, float *G,
+                                     int32_t *status, gdn_stream_t stream);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);

@@ -9,7 +9,7 @@ from gated_deltanet_tree_03_b300 import binding as gb
 
 EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_tree_verify_storeall",
             "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_tree_commit_verify", "gdn_status_str",
-            "gdn_abi_version"}
+            "gdn_abi_version", "gdn_tree_verify_ex", "gdn_tree_commit_ex", "gdn_tree_commit_verify_ex"}
 
 
 def test_header_declares_expected_symbols():
@@ -24,7 +24,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_status_strings_and_version():
-    assert gb.abi_version() == 2
+    assert gb.abi_version() == 3
     for code in (gb.GDN_OK, gb.GDN_EINVAL, gb.GDN_ETOOBIG, gb.GDN_EALIGN, gb.GDN_ECUDA, gb.GDN_EARCH):
         assert gb.status_str(code).startswith("GDN_")
     assert "unknown" in gb.status_str(99)
@@ -84,4 +84,49 @@ def test_accept_host_checks(kw, code):
     rc = gb.library().gdn_tree_accept_greedy(*[args[x] for x in ("draft", "target", "parent", "cu_nodes", "B", "T",
                                                                  "max_nodes", "max_path", "path", "path_len",
                                                                  "status")], None)
+    assert rc == code
+
+
+def _layout(**kw):
+    f = dict(state_slot=None, n_slots=0, H_qk=0, q_scale=1.0, a_raw=None, b_raw=None, A_log=None, dt_bias=None)
+    f.update(kw)
+    return gb.GdnLayout(f["state_slot"], f["n_slots"], f["H_qk"], f["q_scale"], f["a_raw"], f["b_raw"], f["A_log"],
+                        f["dt_bias"])
+
+
+GATES = dict(a_raw=FAKE, b_raw=FAKE, A_log=FAKE, dt_bias=FAKE)
+
+
+@pytest.mark.parametrize("lay,kw,code", [
+    (dict(H_qk=3), {}, gb.GDN_EINVAL),                       # 4 value heads are not a multiple of 3
+    (dict(H_qk=-1), {}, gb.GDN_EINVAL),
+    (dict(state_slot=FAKE, n_slots=0), {}, gb.GDN_EINVAL),  # a pool needs its size
+    (dict(state_slot=FAKE + 4, n_slots=8), {}, gb.GDN_EALIGN),
+    (dict(q_scale=float("inf")), {}, gb.GDN_EINVAL),
+    (dict(q_scale=float("nan")), {}, gb.GDN_EINVAL),
+    (dict(a_raw=FAKE), {}, gb.GDN_EINVAL),                   # some but not all gate arrays
+    (dict(GATES, dt_bias=FAKE + 8), {}, gb.GDN_EALIGN),
+    (dict(GATES), dict(beta=None, g=None, B=0), gb.GDN_OK),   # fused gates: beta and g are not read
+    ({}, dict(beta=None), gb.GDN_EINVAL),                    # ... but are required otherwise
+    (dict(H_qk=2, state_slot=FAKE, n_slots=3, q_scale=0.0), dict(B=0), gb.GDN_OK),
+])
+def test_verify_ex_layout_host_checks(lay, kw, code):
+    args = dict(ST=FAKE, q=FAKE, k=FAKE, v=FAKE, beta=FAKE, g=FAKE, parent=FAKE, cu_nodes=FAKE, B=1, H=4, T=4,
+                d_k=32, d_v=32, max_nodes=4, o=FAKE, U=FAKE, G=FAKE, status=None)
+    args.update(kw)
+    L = _layout(**lay)
+    order = ("ST", "q", "k", "v", "beta", "g", "parent", "cu_nodes", "B", "H", "T", "d_k", "d_v", "max_nodes")
+    rc = gb.library().gdn_tree_verify_ex(*[args[x] for x in order], ctypes.byref(L), args["o"], args["U"],
+                                         args["G"], args["status"], None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("lay,code", [
+    (dict(H_qk=3), gb.GDN_EINVAL), (dict(state_slot=FAKE, n_slots=-2), gb.GDN_EINVAL),
+    (dict(q_scale=float("inf"), a_raw=FAKE), gb.GDN_OK),  # commit ignores the scale and the gates
+])
+def test_commit_ex_layout_host_checks(lay, code):
+    L = _layout(**lay)
+    rc = gb.library().gdn_tree_commit_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 4, 32, 32, 4,
+                                         ctypes.byref(L), None, None)
     assert rc == code
