@@ -413,6 +413,44 @@ def run_ours(args):
                 "traffic": ncu_traffic(dom, wl), "nominal_peak": NOMINAL_HBM_GBS,
                 "frac_of_nominal": kernels[dom]["GB/s"] / NOMINAL_HBM_GBS}
 
+    # draft budgeting on the device: top-B positions (7 drafts per request, 3 per request on
+    # average) and best-first growth over a ternary candidate tree of depth 7, at the batch size
+    budget = None
+    if args.budget:
+        from gated_deltanet_tree_03_b300 import workloads as W
+        rng = np.random.default_rng(77)
+        R = tb0.B
+        pa = torch.from_numpy(W.draw_acceptance(rng, R, 7)).to(dev)
+        pe = torch.from_numpy(W.draw_edge_probs(rng, R, 3, 7)).to(dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        n_sel, cu_b, par_b = torch.empty(R, **i32), torch.empty(R + 1, **i32), torch.empty(R + 3 * R, **i32)
+        n_g, pl_g = torch.empty(R, **i32), torch.empty(R * 64, **i32)
+        cu_g, par_g = torch.empty(R + 1, **i32), torch.empty(R * 64, **i32)
+        st_b = torch.zeros(4, **i32)
+        calls = {"topb": lambda: gb.gdn_tree_budget_topb(pa, R, 7, 3 * R, n_sel, None, cu_b, par_b, st_b, stream),
+                 "grow": lambda: gb.gdn_tree_grow_best_first(pe, R, 3, 7, 0.02, 64, n_g, pl_g, None, None, cu_g,
+                                                             par_g, st_b, stream)}
+        budget = {}
+        for name, fn in calls.items():
+            for _ in range(5):
+                fn()
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            nb = 200
+            b0.record(stream)
+            for _ in range(nb):
+                fn()
+            b1.record(stream)
+            torch.cuda.synchronize()
+            budget[name] = {"ms": b0.elapsed_time(b1) / nb}
+        if int(st_b[0].item()):
+            raise RuntimeError("device reported data errors in the budget kernels")
+        budget["topb"].update(requests=R, positions=7, budget=3 * R, launches=1,
+                              selected=int(n_sel.sum().item()))
+        budget["grow"].update(requests=R, fanout=3, depth=7, candidates=3280, threshold=0.02, max_nodes=64,
+                              launches=2, mean_nodes=float(n_g.float().mean().item()))
+        budget["note"] = ("latency-bound: one CTA sorts all R x 7 survival keys (top-B); one CTA per request sorts "
+                          "its 3280 candidate keys (growth) plus one packing CTA; bytes moved are negligible")
+
     # end to end: pinned host inputs -> device, verify + commit, outputs -> pinned host
     e2e = None
     if not args.no_e2e:
@@ -490,7 +528,7 @@ def run_ours(args):
                 "frac": kernels["commit_verify"]["frac"], "steps": K, "gpu_launches": K,
                 "note": "gdn_tree_commit_verify: each step commits the previous step's accepted paths and verifies "
                         "the next trees in one pass over the state (deferred commit); same work as verify + commit"},
-            "kernels": kernels, "wall_s_timed": wall}
+            "tree_budget": budget, "kernels": kernels, "wall_s_timed": wall}
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:
@@ -512,6 +550,8 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-budget", dest="budget", action="store_false",
+                    help="skip timing the draft-budgeting kernels (top-B positions, best-first growth)")
     ap.add_argument("--no-fused", dest="fused", action="store_false",
                     help="skip timing gdn_tree_commit_verify (the previous step's commit folded into the next verify)")
     args = ap.parse_args(argv)

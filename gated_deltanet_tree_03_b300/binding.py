@@ -17,7 +17,7 @@ from . import _build
 
 GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
 STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8, 16
-STATUS_PATH_TRUNCATED, STATUS_BAD_SLOT = 32, 64
+STATUS_PATH_TRUNCATED, STATUS_BAD_SLOT, STATUS_BAD_PROB = 32, 64, 128
 MAX_NODES = 64
 
 HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
@@ -60,6 +60,8 @@ _SIGS = {
     "gdn_tree_verify_ex": [_P] * 8 + [_I] * 6 + [_LP] + [_P] * 4 + [_P],
     "gdn_tree_commit_ex": [_P] * 8 + [_I] * 6 + [_LP] + [_P, _P],
     "gdn_tree_commit_verify_ex": [_P] * 8 + [_I] * 2 + [_P] * 7 + [_I] * 6 + [_LP] + [_P] * 4 + [_P],
+    "gdn_tree_budget_topb": [_P] + [_I] * 3 + [_P] * 5 + [_P],
+    "gdn_tree_grow_best_first": [_P] + [_I] * 3 + [ctypes.c_float, _I] + [_P] * 7 + [_P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -205,3 +207,16 @@ def gdn_tree_commit_verify_ex(ST, U_prev, G_prev, k_prev, parent_prev, cu_nodes_
                                           _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(parent), _ptr(cu_nodes), B, H,
                                           T, d_k, d_v, max_nodes, _lay(lay), _ptr(o), _ptr(U), _ptr(G), _ptr(status),
                                           _stream(stream)), "gdn_tree_commit_verify_ex")
+
+
+def gdn_tree_budget_topb(p_accept, R, K, budget, n_sel, survival=None, cu_nodes=None, parent=None, status=None,
+                         stream=None):
+    _check(_lib.gdn_tree_budget_topb(_ptr(p_accept), R, K, budget, _ptr(n_sel), _ptr(survival), _ptr(cu_nodes),
+                                     _ptr(parent), _ptr(status), _stream(stream)), "gdn_tree_budget_topb")
+
+
+def gdn_tree_grow_best_first(p_edge, R, fanout, depth, threshold, max_nodes, n_nodes, parent_local, cand=None,
+                             value=None, cu_nodes=None, parent=None, status=None, stream=None):
+    _check(_lib.gdn_tree_grow_best_first(_ptr(p_edge), R, fanout, depth, float(threshold), max_nodes, _ptr(n_nodes),
+                                         _ptr(parent_local), _ptr(cand), _ptr(value), _ptr(cu_nodes), _ptr(parent),
+                                         _ptr(status), _stream(stream)), "gdn_tree_grow_best_first")

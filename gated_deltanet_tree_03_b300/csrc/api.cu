@@ -11,6 +11,7 @@
 
 #include "gdn_tree.h"
 #include "accept.cuh"
+#include "budget.cuh"
 #include "common.cuh"
 #include "commit.cuh"
 #include "storeall.cuh"
@@ -513,6 +514,59 @@ gdn_status gdn_tree_commit_storeall(float *ST, const float *snapshots, const int
   const long long blocks = (long long)B * H * nchunk;
   if (blocks > 0x7fffffffLL) return GDN_EINVAL;
   commit_storeall_kernel<<<unsigned(blocks), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
+gdn_status gdn_tree_budget_topb(const float *p_accept, int32_t R, int32_t K, int32_t budget, int32_t *n_sel,
+                                float *survival, int32_t *cu_nodes, int32_t *parent, int32_t *status,
+                                gdn_stream_t stream) {
+  if (R < 0 || K < 1 || K > kMaxNodes - 1 || budget < 0) return GDN_EINVAL;
+  if ((long long)R * K > kTopbMaxItems) return GDN_ETOOBIG;
+  if (R == 0) return GDN_OK;
+  if (!p_accept || !n_sel || (parent && !cu_nodes)) return GDN_EINVAL;
+  const void *ptrs[] = {p_accept, n_sel, survival, cu_nodes, parent, status};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_EALIGN;
+  gdn_status st;
+  if ((st = check_device()) != GDN_OK) return st;
+  const size_t smem = size_t(R) * K * 12 + size_t(R) * 4;  // keys, staged probabilities, per-request counts
+  if (cudaFuncSetAttribute(topb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return GDN_ECUDA;
+  TopbArgs a{p_accept, R, K, budget, n_sel, survival, cu_nodes, parent, status};
+  topb_kernel<<<1, kTopbThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return launch_status();
+}
+
+gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fanout, int32_t depth, float threshold,
+                                    int32_t max_nodes, int32_t *n_nodes, int32_t *parent_local, int32_t *cand,
+                                    float *value, int32_t *cu_nodes, int32_t *parent, int32_t *status,
+                                    gdn_stream_t stream) {
+  if (R < 0 || fanout < 1 || depth < 0 || max_nodes < 0 || std::isnan(threshold)) return GDN_EINVAL;
+  if (max_nodes > kMaxNodes || R > 0x7fffffff / (max_nodes > 0 ? max_nodes : 1)) return GDN_ETOOBIG;
+  long long C = 0, width = 1;
+  for (int l = 0; l <= depth; ++l) {
+    C += width;
+    if (C > kGrowMaxCand) return GDN_ETOOBIG;
+    width *= fanout;
+  }
+  if (R == 0) return GDN_OK;
+  if (!p_edge || !n_nodes || !parent_local || (!cu_nodes) != (!parent)) return GDN_EINVAL;
+  const void *ptrs[] = {p_edge, n_nodes, parent_local, cand, value, cu_nodes, parent, status};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_EALIGN;
+  gdn_status st;
+  if ((st = check_device()) != GDN_OK) return st;
+  const size_t smem = size_t(C) * 8 + size_t(C) * 4;  // candidate keys (then output positions), values
+  if (cudaFuncSetAttribute(grow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return GDN_ECUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GrowArgs a{p_edge, R, fanout, depth, int(C), max_nodes, threshold, n_nodes, cand, parent_local, value, status};
+  grow_kernel<<<unsigned(R), kGrowThreads, smem, s>>>(a);
+  if ((st = launch_status()) != GDN_OK || !cu_nodes) return st;
+  PackArgs pa{n_nodes, parent_local, R, max_nodes, cu_nodes, parent};
+  pack_scan_kernel<<<1, kScanThreads, 0, s>>>(pa);
+  if ((st = launch_status()) != GDN_OK) return st;
+  pack_copy_kernel<<<unsigned((R + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0, s>>>(pa);
   return launch_status();
 }
 

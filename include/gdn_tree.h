@@ -76,6 +76,7 @@ typedef enum gdn_status {
 #define GDN_STATUS_BAD_OFFSETS 16u   /* cu_nodes not non-decreasing inside [0, T]            */
 #define GDN_STATUS_PATH_TRUNCATED 32u /* an accepted path was longer than max_path            */
 #define GDN_STATUS_BAD_SLOT 64u      /* a state slot outside [0, n_slots) and not -1         */
+#define GDN_STATUS_BAD_PROB 128u     /* an estimated probability outside [0, 1] or NaN        */
 
 /*
  * gdn_layout - serving layout of the *_ex entry points: how an inference engine that hosts
@@ -285,6 +286,58 @@ gdn_status gdn_tree_commit_verify_ex(float *ST, const float *U_prev, const float
                                      int32_t d_k, int32_t d_v, int32_t max_nodes,
                                      const gdn_layout *layout, float *o, float *U, float *G,
                                      int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_budget_topb - adaptive verification budget (DSpark adaptive-verification news item:
+ * each draft token's estimated probability of passing verification gives, per request, the
+ * probability that its sequence survives to each position; one global budget B goes to the
+ * positions with the largest survival probabilities across all requests).
+ *
+ *   p_accept  [R][K] fp32  in   estimated acceptance probability of draft position i of
+ *                               request r; values outside [0, 1] or NaN count as 0 and set
+ *                               GDN_STATUS_BAD_PROB
+ *   R, K, budget           in   requests, draft positions per request (1..63), positions to
+ *                               verify in total (>= 0); R * K <= 16384
+ *   n_sel     [R]    out        positions chosen for request r - always its first n_sel[r]
+ *   survival  [R][K] out        optional: s[r][i] = p[r][0] * ... * p[r][i] (fp32, in that order)
+ *   cu_nodes  [R+1]  out        optional: the verify batch, one chain per request of 1 + n_sel[r]
+ *                               nodes (the token the target already produced, then the drafts)
+ *   parent    [R + min(budget, R K)] out   optional (needs cu_nodes): the chains' parents
+ * Order: survival descending, equal values by (request, position) ascending; the choice is
+ * exact (fp32 products, compared as numbers). One CTA; the result is a function of the inputs.
+ */
+gdn_status gdn_tree_budget_topb(const float *p_accept, int32_t R, int32_t K, int32_t budget,
+                                int32_t *n_sel, float *survival, int32_t *cu_nodes,
+                                int32_t *parent, int32_t *status, gdn_stream_t stream);
+
+/*
+ * gdn_tree_grow_best_first - threshold best-first draft-tree growth (TreeSpark page: the tree
+ * grows along its most promising branch first and stops when the value of the best remaining
+ * candidate drops below a threshold; a candidate's value is the survival product along its
+ * branch).
+ *
+ * Candidates per request form a complete fanout-ary tree of the given depth, numbered
+ * breadth-first: 0 is the root (the token the target already produced, value 1, always
+ * taken), the children of c are fanout*c + 1 .. fanout*c + fanout, C = sum_l fanout^l <= 8192.
+ *   p_edge [R][C] fp32  in   estimated probability that candidate c is accepted given its
+ *                            parent (column 0 unused); invalid values count as 0 (BAD_PROB)
+ *   threshold           in   a candidate is taken while its value >= threshold
+ *   max_nodes           in   at most this many nodes per request (0..64)
+ *   n_nodes      [R]              out  nodes taken per request
+ *   parent_local [R][max_nodes]   out  request-local parent of each taken node, in the order
+ *                                      taken (parent before child), -1 for the root and past n
+ *   cand, value  [R][max_nodes]   out  optional: candidate index and value of each taken node
+ *                                      (-1 / 0 past n)
+ *   cu_nodes [R+1], parent [R * max_nodes]   out  optional (both or neither): the same trees
+ *                                      packed as a ragged verify batch
+ * The order taken is value descending, equal values by candidate index ascending, which is
+ * the best-first order because values never grow along a branch.
+ */
+gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fanout, int32_t depth,
+                                    float threshold, int32_t max_nodes, int32_t *n_nodes,
+                                    int32_t *parent_local, int32_t *cand, float *value,
+                                    int32_t *cu_nodes, int32_t *parent, int32_t *status,
+                                    gdn_stream_t stream);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);

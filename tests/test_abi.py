@@ -9,7 +9,8 @@ from gated_deltanet_tree_03_b300 import binding as gb
 
 EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_tree_verify_storeall",
             "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_tree_commit_verify", "gdn_status_str",
-            "gdn_abi_version", "gdn_tree_verify_ex", "gdn_tree_commit_ex", "gdn_tree_commit_verify_ex"}
+            "gdn_abi_version", "gdn_tree_verify_ex", "gdn_tree_commit_ex", "gdn_tree_commit_verify_ex",
+            "gdn_tree_budget_topb", "gdn_tree_grow_best_first"}
 
 
 def test_header_declares_expected_symbols():
@@ -129,4 +130,30 @@ def test_commit_ex_layout_host_checks(lay, code):
     L = _layout(**lay)
     rc = gb.library().gdn_tree_commit_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 4, 32, 32, 4,
                                          ctypes.byref(L), None, None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), gb.GDN_EINVAL), (dict(K=64), gb.GDN_EINVAL), (dict(budget=-1), gb.GDN_EINVAL),
+    (dict(R=2341, K=7), gb.GDN_ETOOBIG), (dict(p=None), gb.GDN_EINVAL), (dict(n_sel=FAKE + 4), gb.GDN_EALIGN),
+    (dict(cu=None), gb.GDN_EINVAL),  # parent without cu_nodes
+    (dict(R=0), gb.GDN_OK)])
+def test_budget_topb_host_checks(kw, code):
+    a = dict(p=FAKE, R=4, K=7, budget=5, n_sel=FAKE, surv=None, cu=FAKE, par=FAKE)
+    a.update(kw)
+    rc = gb.library().gdn_tree_budget_topb(a["p"], a["R"], a["K"], a["budget"], a["n_sel"], a["surv"], a["cu"],
+                                           a["par"], None, None)
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(fanout=0), gb.GDN_EINVAL), (dict(depth=-1), gb.GDN_EINVAL), (dict(max_nodes=65), gb.GDN_ETOOBIG),
+    (dict(fanout=2, depth=13), gb.GDN_ETOOBIG), (dict(fanout=4, depth=7), gb.GDN_ETOOBIG),
+    (dict(thr=float("nan")), gb.GDN_EINVAL), (dict(parent=None), gb.GDN_EINVAL),  # cu_nodes without parent
+    (dict(parent_local=None), gb.GDN_EINVAL), (dict(R=0), gb.GDN_OK)])
+def test_grow_host_checks(kw, code):
+    a = dict(p=FAKE, R=4, fanout=3, depth=4, thr=0.1, max_nodes=32, n=FAKE, parent_local=FAKE, cu=FAKE, parent=FAKE)
+    a.update(kw)
+    rc = gb.library().gdn_tree_grow_best_first(a["p"], a["R"], a["fanout"], a["depth"], a["thr"], a["max_nodes"],
+                                               a["n"], a["parent_local"], None, None, a["cu"], a["parent"], None, None)
     assert rc == code
