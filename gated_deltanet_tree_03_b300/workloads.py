@@ -465,3 +465,64 @@ def draw_edge_probs(rng: np.random.Generator, R: int, fanout: int, depth: int, a
     w = -np.sort(-w, axis=2)
     p[:, 1:] = w.reshape(R, n_internal * fanout).astype(np.float32)
     return p
+
+
+@dataclass
+class AttentionBatch:
+    """Inputs of one tree-bias attention layer (see ``make_attention_batch``)."""
+
+    B: int
+    Hq: int
+    Hkv: int
+    d: int
+    parent: np.ndarray     # [T] int32
+    cu_nodes: np.ndarray   # [B+1] int32
+    cu_prefix: np.ndarray  # [B+1] int32
+    q: np.ndarray          # [T, Hq, d] uint16 (bf16 bits)
+    k: np.ndarray          # [T, Hkv, d] uint16
+    v: np.ndarray          # [T, Hkv, d] uint16
+    k_cache: np.ndarray    # [P_total, Hkv, d] uint16
+    v_cache: np.ndarray    # [P_total, Hkv, d] uint16
+    scale: float
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_nodes[-1])
+
+    @property
+    def P(self) -> int:
+        return int(self.cu_prefix[-1])
+
+    @property
+    def max_nodes(self) -> int:
+        return int(np.max(np.diff(self.cu_nodes))) if self.B else 0
+
+    @property
+    def max_prefix(self) -> int:
+        return int(np.max(np.diff(self.cu_prefix))) if self.B else 0
+
+
+def make_attention_batch(seed: int, B: int, Hq: int, Hkv: int, d: int, prefix_range=(0, 512), parents=None,
+                         n_range=(1, 16), fanout_max=3, depth_max=6) -> AttentionBatch:
+    """Tree-bias attention inputs: a committed key/value prefix per request, of length uniform
+    in ``prefix_range``, and a draft tree per request (``parents``, or random trees as in
+    ``make_random_batch``). q, k, v and the caches are N(0, 1) rounded to bf16; the score scale
+    is d^-1/2."""
+    rng = np.random.default_rng([seed, 0xa7])
+    if parents is None:
+        parents = []
+        for _ in range(B):
+            n = int(rng.integers(n_range[0], n_range[1] + 1))
+            parents.append(random_tree_parents(rng, n, fanout_max=fanout_max, depth_max=depth_max))
+    sizes = [len(p) for p in parents]
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(sizes)
+    plen = rng.integers(prefix_range[0], prefix_range[1] + 1, size=B)
+    cp = np.zeros(B + 1, dtype=np.int32)
+    cp[1:] = np.cumsum(plen)
+    T, P = int(cu[-1]), int(cp[-1])
+    bf = lambda *shape: f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))
+    parent = np.concatenate([np.asarray(p, np.int32) for p in parents]) if T else np.zeros(0, np.int32)
+    return AttentionBatch(B=B, Hq=Hq, Hkv=Hkv, d=d, parent=parent, cu_nodes=cu, cu_prefix=cp,
+                          q=bf(T, Hq, d), k=bf(T, Hkv, d), v=bf(T, Hkv, d), k_cache=bf(P, Hkv, d),
+                          v_cache=bf(P, Hkv, d), scale=float(d ** -0.5))
