@@ -67,13 +67,33 @@ def fused_bytes(tb) -> int:
     return verify_bytes(tb) + commit_bytes(tb) - active * tb.H * tb.dk * tb.dv * 4
 
 
+def attention_bytes(ab) -> int:
+    """Tree-bias attention: every prefix key and value read once per (request, key/value head),
+    the draft nodes' q, k, v read once, o (fp32) written once."""
+    return (2 * ab.P * ab.Hkv * ab.d * 2 + ab.T * ab.Hq * ab.d * 2 + 2 * ab.T * ab.Hkv * ab.d * 2
+            + ab.T * ab.Hq * ab.d * 4 + ab.T * 4 + 2 * (ab.B + 1) * 4)
+
+
+def attention_flops(ab) -> int:
+    """Useful multiply-adds x 2 of Q.K^T and P.V: per query row, (prefix + root-path) keys."""
+    depth = np.zeros(ab.T, np.int64)
+    for r in range(ab.B):
+        t0 = int(ab.cu_nodes[r])
+        for t in range(int(ab.cu_nodes[r + 1]) - t0):
+            p = int(ab.parent[t0 + t])
+            depth[t0 + t] = 1 if p < 0 else depth[t0 + p] + 1
+    plen = np.repeat(np.diff(ab.cu_prefix), np.diff(ab.cu_nodes))
+    return int(4 * ab.d * ab.Hq * np.sum(plen + depth))
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6400.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1800.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "source": "fallback"}
 
 
 def kernel_src_sha(kernel: str) -> str:
@@ -451,6 +471,50 @@ def run_ours(args):
         budget["note"] = ("latency-bound: one CTA sorts all R x 7 survival keys (top-B); one CTA per request sorts "
                           "its 3280 candidate keys (growth) plus one packing CTA; bytes moved are negligible")
 
+    # tree-bias attention of the model's attention layers over the same kind of trees: 4096-key
+    # committed prefixes, 16 query heads on 2 key/value heads, d = 128
+    attention = None
+    if args.attention:
+        from gated_deltanet_tree_03_b300 import workloads as W
+        attention = {}
+        R = 64
+        shapes = {"rootbranch6": [W.root_branch_parents()] * R,
+                  "tree32": [W.random_tree_parents(np.random.default_rng(500 + i), 32, 3, 6) for i in range(R)]}
+        for name, parents in shapes.items():
+            ab = W.make_attention_batch(31, B=R, Hq=16, Hkv=2, d=128, prefix_range=(4096, 4096), parents=parents)
+            bf = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).to(dev)
+            i32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(dev)
+            ins = [bf(ab.q), bf(ab.k), bf(ab.v), bf(ab.k_cache), bf(ab.v_cache), i32(ab.cu_prefix), i32(ab.parent),
+                   i32(ab.cu_nodes)]
+            o_a = torch.empty((ab.T, ab.Hq, ab.d), device=dev)
+            wsb = gb.gdn_tree_attention_workspace_size(R, 16, 2, 128, ab.max_nodes, ab.max_prefix)
+            ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+            st_a = torch.zeros(4, dtype=torch.int32, device=dev)
+            fn = lambda: gb.gdn_tree_attention(*ins, R, 16, 2, ab.T, ab.P, 128, ab.max_nodes, ab.max_prefix, ab.scale,
+                                               o_a, ws, wsb, st_a, stream)
+            for _ in range(5):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            na = 50
+            a0.record(stream)
+            for _ in range(na):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            if int(st_a[0].item()):
+                raise RuntimeError("device reported data errors in tree attention")
+            ms = a0.elapsed_time(a1) / na
+            ab_bytes, ab_flops = attention_bytes(ab), attention_flops(ab)
+            attention[name] = {"ms": ms, "requests": R, "nodes": ab.T, "prefix_per_request": 4096, "heads_q": 16,
+                               "heads_kv": 2, "d": 128, "workspace_bytes": wsb, "alg_bytes": ab_bytes,
+                               "GB/s": ab_bytes / (ms * 1e6), "frac_hbm": ab_bytes / (ms * 1e6) / peaks["hbm_gbs"],
+                               "useful_TFLOP/s": ab_flops / (ms * 1e9),
+                               "frac_bf16": ab_flops / (ms * 1e9) / peaks["bf16_tflops"]}
+            del ins, o_a, ws
+        attention["note"] = ("gdn_tree_attention: each draft node attends to its request's committed prefix and "
+                             "its own root-to-node path; K/V caches 268 MB (> L2); frac_hbm against the measured "
+                             "copy bandwidth, frac_bf16 (useful flops) against the measured bf16 GEMM burst")
+
     # end to end: pinned host inputs -> device, verify + commit, outputs -> pinned host
     e2e = None
     if not args.no_e2e:
@@ -528,7 +592,7 @@ def run_ours(args):
                 "frac": kernels["commit_verify"]["frac"], "steps": K, "gpu_launches": K,
                 "note": "gdn_tree_commit_verify: each step commits the previous step's accepted paths and verifies "
                         "the next trees in one pass over the state (deferred commit); same work as verify + commit"},
-            "tree_budget": budget, "kernels": kernels, "wall_s_timed": wall}
+            "tree_budget": budget, "tree_attention": attention, "kernels": kernels, "wall_s_timed": wall}
     if rank == 0:
         print(json.dumps(line))
     if dist is not None:
@@ -550,6 +614,8 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-attention", dest="attention", action="store_false",
+                    help="skip timing tree-bias attention (gdn_tree_attention)")
     ap.add_argument("--no-budget", dest="budget", action="store_false",
                     help="skip timing the draft-budgeting kernels (top-B positions, best-first growth)")
     ap.add_argument("--no-fused", dest="fused", action="store_false",

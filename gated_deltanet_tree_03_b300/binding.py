@@ -62,11 +62,14 @@ _SIGS = {
     "gdn_tree_commit_verify_ex": [_P] * 8 + [_I] * 2 + [_P] * 7 + [_I] * 6 + [_LP] + [_P] * 4 + [_P],
     "gdn_tree_budget_topb": [_P] + [_I] * 3 + [_P] * 5 + [_P],
     "gdn_tree_grow_best_first": [_P] + [_I] * 3 + [ctypes.c_float, _I] + [_P] * 7 + [_P],
+    "gdn_tree_attention": [_P] * 8 + [_I] * 8 + [ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+_lib.gdn_tree_attention_workspace_size.argtypes = [_I] * 6
+_lib.gdn_tree_attention_workspace_size.restype = ctypes.c_size_t
 _lib.gdn_status_str.argtypes = [ctypes.c_int]
 _lib.gdn_status_str.restype = ctypes.c_char_p
 _lib.gdn_abi_version.argtypes = []
@@ -220,3 +223,17 @@ def gdn_tree_grow_best_first(p_edge, R, fanout, depth, threshold, max_nodes, n_n
     _check(_lib.gdn_tree_grow_best_first(_ptr(p_edge), R, fanout, depth, float(threshold), max_nodes, _ptr(n_nodes),
                                          _ptr(parent_local), _ptr(cand), _ptr(value), _ptr(cu_nodes), _ptr(parent),
                                          _ptr(status), _stream(stream)), "gdn_tree_grow_best_first")
+
+
+def gdn_tree_attention_workspace_size(B, H_q, H_kv, d, max_nodes, max_prefix) -> int:
+    return int(_lib.gdn_tree_attention_workspace_size(B, H_q, H_kv, d, max_nodes, max_prefix))
+
+
+def gdn_tree_attention(q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, B, H_q, H_kv, T, P_total, d, max_nodes,
+                       max_prefix, scale, o, workspace=None, workspace_bytes=0, status=None, stream=None):
+    if workspace is not None and hasattr(workspace, "numel") and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib.gdn_tree_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_prefix),
+                                   _ptr(parent), _ptr(cu_nodes), B, H_q, H_kv, T, P_total, d, max_nodes, max_prefix,
+                                   float(scale), _ptr(o), _ptr(workspace), int(workspace_bytes), _ptr(status),
+                                   _stream(stream)), "gdn_tree_attention")

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/gdn_tree.h: argument checks, launch
 // configuration, TMA descriptor encoding and kernel dispatch. Nothing here allocates device
 // memory, synchronises the device or keeps per-call state.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -11,6 +12,7 @@
 
 #include "gdn_tree.h"
 #include "accept.cuh"
+#include "attention.cuh"
 #include "budget.cuh"
 #include "common.cuh"
 #include "commit.cuh"
@@ -147,6 +149,19 @@ bool encode_rows(CUtensorMap *map, const uint16_t *base, int D, int H, int T, in
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [T][H][D] bf16 rows viewed as (D, H, T); box = (box0, box_h, rows), 128-byte swizzle
+bool encode_rows_box(CUtensorMap *map, const uint16_t *base, int D, int H, int T, int box0, int box_h, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(H), cuuint64_t(T)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(H) * D * 2};
+  const cuuint32_t box[3] = {cuuint32_t(box0), cuuint32_t(box_h), cuuint32_t(rows)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -359,6 +374,77 @@ gdn_status commit_verify_impl(float *ST, const float *U_prev, const float *G_pre
   return launch_verify_stream_dims<true>(a, c, L, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ tree-bias attention
+struct AttnPlan {
+  int G = 0, tiles = 0, splits = 1, blocks_per_split = 1;
+  size_t ws_bytes = 0;  // workspace the plan needs (0 with one split)
+};
+
+int attn_sms() {
+  const int n = sm_count();
+  return n > 0 ? n : 148;
+}
+
+// Query tiles per (request, head) and key splits: split the prefix only when the (request,
+// head, tile) grid is smaller than two CTAs per SM, and only as far as `ws_limit` bytes allow.
+AttnPlan attn_plan(int B, int Hq, int Hkv, int d, int max_nodes, int max_prefix, size_t ws_limit) {
+  AttnPlan p;
+  p.G = Hq / Hkv;
+  p.tiles = (max_nodes * p.G + kAttnRows - 1) / kAttnRows;
+  if (p.tiles < 1) p.tiles = 1;
+  const long long base = (long long)B * Hkv * p.tiles;
+  const int nblk = (max_prefix + kAttnKeys - 1) / kAttnKeys;
+  const int target = 2 * attn_sms();
+  int splits = 1;
+  if (base < target && nblk > 1) splits = int(std::min<long long>(nblk, (target + base - 1) / base));
+  const size_t per_split = size_t(base) * kAttnRows * size_t(d + 2) * 4;
+  if (splits > 1 && per_split * splits > ws_limit) splits = int(ws_limit / per_split);
+  if (splits < 2) splits = 1;
+  const int bps = nblk > 0 ? (nblk + splits - 1) / splits : 1;
+  p.splits = nblk > 0 ? (nblk + bps - 1) / bps : 1;
+  p.blocks_per_split = bps;
+  p.ws_bytes = p.splits > 1 ? per_split * p.splits : 0;
+  return p;
+}
+
+gdn_status check_attn_shape(int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t max_nodes, int32_t max_prefix) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_nodes < 0 || max_prefix < 0) return GDN_EINVAL;
+  if (Hq % Hkv != 0) return GDN_EINVAL;
+  const int G = Hq / Hkv;
+  if (G > kAttnRows || (G & (G - 1)) != 0) return GDN_EINVAL;  // whole nodes per 128-row tile
+  if (d != 64 && d != 128) return GDN_EINVAL;
+  if (max_nodes > kMaxNodes) return GDN_ETOOBIG;
+  if (B > 65535 || Hkv > 65535) return GDN_EINVAL;
+  return GDN_OK;
+}
+
+template <int D>
+gdn_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const AttnArgs &a, cudaStream_t s) {
+  CUtensorMap tq, tkc, tvc, tkt, tvt;
+  const bool have_prefix = a.P_total > 0 && k_cache && v_cache;
+  // without a prefix the cache maps are never read; they describe the node arrays instead
+  const uint16_t *kc = have_prefix ? k_cache : k, *vc = have_prefix ? v_cache : v;
+  const int pt = have_prefix ? a.P_total : a.T;
+  if (!encode_rows_box(&tq, q, D, a.Hq, a.T, 64, a.G, kAttnRows / a.G) ||
+      !encode_rows(&tkc, kc, D, a.Hkv, pt, 64, kAttnKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tvc, vc, D, a.Hkv, pt, 64, kAttnKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tkt, k, D, a.Hkv, a.T, 64, kAttnTreeKeys, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&tvt, v, D, a.Hkv, a.T, 64, kAttnTreeKeys, CU_TENSOR_MAP_SWIZZLE_128B))
+    return GDN_ECUDA;
+  const uint32_t smem = attn_smem_bytes(D);
+  if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+      cudaSuccess)
+    return GDN_ECUDA;
+  dim3 grid(unsigned(a.tiles * a.splits), unsigned(a.Hkv), unsigned(a.B));
+  tree_attention_kernel<D><<<grid, kAttnThreads, smem, s>>>(tq, tkc, tvc, tkt, tvt, a);
+  gdn_status st = launch_status();
+  if (st != GDN_OK || a.splits == 1) return st;
+  dim3 cgrid(unsigned(a.B * a.Hkv * a.tiles), unsigned(kAttnRows / 8));
+  tree_attention_combine_kernel<D><<<cgrid, 256, 0, s>>>(a);
+  return launch_status();
+}
+
 }  // namespace
 
 extern "C" {
@@ -568,6 +654,41 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
   if ((st = launch_status()) != GDN_OK) return st;
   pack_copy_kernel<<<unsigned((R + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0, s>>>(pa);
   return launch_status();
+}
+
+size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t max_nodes,
+                                         int32_t max_prefix) {
+  if (check_attn_shape(B, H_q, H_kv, d, max_nodes, max_prefix) != GDN_OK || B == 0) return 0;
+  return attn_plan(B, H_q, H_kv, d, max_nodes, max_prefix, ~size_t(0)).ws_bytes;
+}
+
+gdn_status gdn_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *cu_prefix, const int32_t *parent,
+                              const int32_t *cu_nodes, int32_t B, int32_t H_q, int32_t H_kv, int32_t T,
+                              int32_t P_total, int32_t d, int32_t max_nodes, int32_t max_prefix, float scale, float *o,
+                              void *workspace, size_t workspace_bytes, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_attn_shape(B, H_q, H_kv, d, max_nodes, max_prefix);
+  if (st != GDN_OK) return st;
+  if (T < 0 || P_total < 0 || !std::isfinite(scale)) return GDN_EINVAL;
+  if (B == 0 || T == 0 || max_nodes == 0) return GDN_OK;
+  if (!q || !k || !v || !cu_prefix || !parent || !cu_nodes || !o) return GDN_EINVAL;
+  if (P_total > 0 && (!k_cache || !v_cache)) return GDN_EINVAL;
+  const void *ptrs[] = {q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, o, workspace, status};
+  for (const void *p : ptrs)
+    if (p && !aligned16(p)) return GDN_EALIGN;
+  if ((st = check_device()) != GDN_OK) return st;
+  const AttnPlan plan = attn_plan(B, H_q, H_kv, d, max_nodes, max_prefix, workspace ? workspace_bytes : 0);
+  if ((long long)plan.tiles * plan.splits > 0x7fffffffLL) return GDN_EINVAL;
+  AttnArgs a{parent, cu_nodes, cu_prefix, B, H_q, H_kv, plan.G, T, P_total, max_nodes, max_prefix,
+             plan.tiles, plan.splits, plan.blocks_per_split, scale * 1.4426950408889634f, o, nullptr, nullptr,
+             status};
+  if (plan.splits > 1) {  // partial outputs first, then the (max, sum) pairs
+    a.ws_o = static_cast<float *>(workspace);
+    a.ws_ml = a.ws_o + plan.ws_bytes / 4 / size_t(d + 2) * size_t(d);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_attention<128>(q, k, v, k_cache, v_cache, a, s)
+                  : launch_attention<64>(q, k, v, k_cache, v_cache, a, s);
 }
 
 }  // extern "C"

@@ -146,6 +146,22 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, float (&out)[
   for (int i = 0; i < 16; ++i) out[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 16 columns of 32-bit TMEM words from this thread's registers (lane base + i <- thread
+// i); returns once the stores have completed.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const float (&in)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(in[0])), "r"(__float_as_uint(in[1])), "r"(__float_as_uint(in[2])),
+      "r"(__float_as_uint(in[3])), "r"(__float_as_uint(in[4])), "r"(__float_as_uint(in[5])),
+      "r"(__float_as_uint(in[6])), "r"(__float_as_uint(in[7])), "r"(__float_as_uint(in[8])),
+      "r"(__float_as_uint(in[9])), "r"(__float_as_uint(in[10])), "r"(__float_as_uint(in[11])),
+      "r"(__float_as_uint(in[12])), "r"(__float_as_uint(in[13])), "r"(__float_as_uint(in[14])),
+      "r"(__float_as_uint(in[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout (8-row x 128-byte
 // atoms, 1024 bytes apart along M/N). `saddr` is the shared address of the first element of the
 // K-slice; it may be offset by 32-byte steps inside an atom to select K = 16 bf16 slices.
@@ -153,6 +169,18 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return uint64_t((saddr & 0x3FFFFu) >> 4)  // start address, 16-byte units
          | (uint64_t(1) << 16)              // leading byte offset (unused for swizzled K-major)
          | (uint64_t(1024 >> 4) << 32)      // stride byte offset: next 8-row group
+         | (uint64_t(1) << 46)              // descriptor version for sm_100-class
+         | (uint64_t(2) << 61);             // 128-byte swizzle
+}
+
+// Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzle layout, as a TMA
+// copy with 128-byte swizzle lays out rows of 64 bf16 along N, one row per K index: 8 K-rows x
+// 128 bytes per 1024-byte atom, atoms 1024 bytes apart along K. Used with N = 64 (one atom along
+// N), so the stride between atoms along N never enters; both offset fields hold the K stride.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4)  // start address, 16-byte units
+         | (uint64_t(1024 >> 4) << 16)      // leading byte offset
+         | (uint64_t(1024 >> 4) << 32)      // stride byte offset
          | (uint64_t(1) << 46)              // descriptor version for sm_100-class
          | (uint64_t(2) << 61);             // 128-byte swizzle
 }
@@ -165,6 +193,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (uint32_t(N >> 3) << 17)    // N / 8
          | (uint32_t(M >> 4) << 24);   // M / 16
 }
+
+// The same with B MN-major (B stored with N contiguous, as a row-major [K][N] tile).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 16); }
 
 }  // namespace ptx
 }  // namespace gdn

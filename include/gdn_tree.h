@@ -49,6 +49,7 @@
 #ifndef GDN_TREE_H
 #define GDN_TREE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -338,6 +339,47 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
                                     int32_t *parent_local, int32_t *cand, float *value,
                                     int32_t *cu_nodes, int32_t *parent, int32_t *status,
                                     gdn_stream_t stream);
+
+/*
+ * gdn_tree_attention - tree-bias attention for the attention layers of a hybrid model (GDN
+ * Tree-Scan abstract: tree-bias attention beside the recurrent-state replay; an attention-only
+ * verifier mainly needs the ancestry mask). Draft node t of request r, query head h (key/value
+ * head h / (H_q / H_kv)), attends to every key of the request's committed prefix and to the
+ * draft nodes on its own root-to-node path, itself included:
+ *     o[t][h] = sum_j softmax_j(scale * q[t][h] . k_j) v_j   over those keys j
+ *
+ *   q        [T][H_q][d]        bf16  in   the draft nodes' queries
+ *   k, v     [T][H_kv][d]       bf16  in   the draft nodes' own keys and values
+ *   k_cache, v_cache [P_total][H_kv][d] bf16 in   committed prefixes; request r owns rows
+ *                                          cu_prefix[r] .. cu_prefix[r+1]-1 (may be NULL when
+ *                                          P_total is 0)
+ *   cu_prefix [B+1], parent [T], cu_nodes [B+1] int32 in   as for gdn_tree_verify; at most
+ *                                          max_nodes (<= 64) nodes and max_prefix keys per request
+ *   d                                 64 or 128; H_q / H_kv a power of two <= 128
+ *   scale                             score scale (e.g. d^-1/2)
+ *   o        [T][H_q][d]        fp32  out  written for every node of every valid request
+ *   workspace, workspace_bytes        optional device scratch: with too few (request, head)
+ *                                     pairs to fill the GPU, long prefixes are split across CTAs
+ *                                     and merged, using up to gdn_tree_attention_workspace_size()
+ *                                     bytes of it; with NULL or less, fewer splits (none) are made
+ *   status                            optional: BAD_OFFSETS (offsets outside T / P_total, or a
+ *                                     prefix longer than max_prefix), TOO_MANY_NODES, BAD_TREE,
+ *                                     TIMEOUT; the request then writes nothing
+ * Scores and the running softmax are fp32; the probabilities enter P.V rounded to bf16 (the
+ * tensor-core operand type), so |o - o_exact| <= 2^-8 max|v| per output.
+ */
+gdn_status gdn_tree_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const uint16_t *k_cache, const uint16_t *v_cache,
+                              const int32_t *cu_prefix, const int32_t *parent,
+                              const int32_t *cu_nodes, int32_t B, int32_t H_q, int32_t H_kv,
+                              int32_t T, int32_t P_total, int32_t d, int32_t max_nodes,
+                              int32_t max_prefix, float scale, float *o, void *workspace,
+                              size_t workspace_bytes, int32_t *status, gdn_stream_t stream);
+
+/* Workspace bytes gdn_tree_attention uses at most for these sizes on the current device (0 when
+ * it would not split). */
+size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t d,
+                                         int32_t max_nodes, int32_t max_prefix);
 
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);

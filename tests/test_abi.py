@@ -10,7 +10,8 @@ from gated_deltanet_tree_03_b300 import binding as gb
 EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_tree_verify_storeall",
             "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_tree_commit_verify", "gdn_status_str",
             "gdn_abi_version", "gdn_tree_verify_ex", "gdn_tree_commit_ex", "gdn_tree_commit_verify_ex",
-            "gdn_tree_budget_topb", "gdn_tree_grow_best_first"}
+            "gdn_tree_budget_topb", "gdn_tree_grow_best_first", "gdn_tree_attention",
+            "gdn_tree_attention_workspace_size"}
 
 
 def test_header_declares_expected_symbols():
@@ -157,3 +158,29 @@ def test_grow_host_checks(kw, code):
     rc = gb.library().gdn_tree_grow_best_first(a["p"], a["R"], a["fanout"], a["depth"], a["thr"], a["max_nodes"],
                                                a["n"], a["parent_local"], None, None, a["cu"], a["parent"], None, None)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=12, Hkv=4), gb.GDN_EINVAL),  # group of 3 query heads: not a power of two
+    (dict(Hq=6, Hkv=4), gb.GDN_EINVAL), (dict(d=32), gb.GDN_EINVAL), (dict(max_nodes=65), gb.GDN_ETOOBIG),
+    (dict(scale=float("inf")), gb.GDN_EINVAL), (dict(q=None), gb.GDN_EINVAL), (dict(kc=None), gb.GDN_EINVAL),
+    (dict(o=FAKE + 4), gb.GDN_EALIGN), (dict(B=0), gb.GDN_OK), (dict(max_nodes=0), gb.GDN_OK),
+    (dict(kc=None, vc=None, P=0), gb.GDN_ECUDA)])  # valid arguments: only the missing GPU stops it
+def test_attention_host_checks(kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cp=FAKE, par=FAKE, cu=FAKE, B=2, Hq=16, Hkv=2, T=8, P=64, d=128,
+             max_nodes=4, max_prefix=32, scale=0.1, o=FAKE)
+    a.update(kw)
+    rc = gb.library().gdn_tree_attention(a["q"], a["k"], a["v"], a["kc"], a["vc"], a["cp"], a["par"], a["cu"], a["B"],
+                                         a["Hq"], a["Hkv"], a["T"], a["P"], a["d"], a["max_nodes"], a["max_prefix"],
+                                         ctypes.c_float(a["scale"]), a["o"], None, 0, None, None)
+    if code == gb.GDN_ECUDA:
+        assert rc in (gb.GDN_ECUDA, gb.GDN_EARCH)
+    else:
+        assert rc == code
+
+
+def test_attention_workspace_size_is_zero_without_splits():
+    assert gb.gdn_tree_attention_workspace_size(0, 16, 2, 128, 8, 4096) == 0
+    assert gb.gdn_tree_attention_workspace_size(4, 16, 2, 128, 8, 100) == 0  # one key block: nothing to split
+    big = gb.gdn_tree_attention_workspace_size(1, 16, 2, 128, 6, 8192)
+    assert big > 0 and big % (128 * 130 * 4) == 0
