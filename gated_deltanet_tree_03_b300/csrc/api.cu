@@ -669,7 +669,7 @@ gdn_status gdn_tree_attention(const uint16_t *q, const uint16_t *k, const uint16
                               void *workspace, size_t workspace_bytes, int32_t *status, gdn_stream_t stream) {
   gdn_status st = check_attn_shape(B, H_q, H_kv, d, max_nodes, max_prefix);
   if (st != GDN_OK) return st;
-  if (T < 0 || P_total < 0 || !std::isfinite(scale)) return GDN_EINVAL;
+  if (T < 0 || P_total < 0 || !std::isfinite(scale) || !(scale > 0.f)) return GDN_EINVAL;
   if (B == 0 || T == 0 || max_nodes == 0) return GDN_OK;
   if (!q || !k || !v || !cu_prefix || !parent || !cu_nodes || !o) return GDN_EINVAL;
   if (P_total > 0 && (!k_cache || !v_cache)) return GDN_EINVAL;

@@ -12,9 +12,13 @@
 //                      scores are computed while this block's softmax runs)
 //     softmax          one thread per query row: mask (prefix length / ancestor bits), running
 //                      max and sum in the log2 domain, O rescaled in tensor memory when the max
-//                      grows, probabilities written to shared memory as bf16
-//     O += P V         tcgen05.mma with V read as an MN-major operand straight from its TMA tile
-// Warp roles: 0 TMA producer, 1 MMA issuer, 2 tree masks, 4..7 softmax and epilogue.
+//                      grows, probabilities written back as bf16 over the S columns they came from
+//     O += P V         tcgen05.mma with P read from tensor memory and V read as an MN-major
+//                      operand straight from its TMA tile
+// Warp roles: 0 key (and query) TMA producer, 1 MMA issuer (issues whichever of the next S and
+// the next P.V is ready), 2 tree masks, 3 value TMA producer, 4..7 softmax and epilogue.
+// A row's running max is only moved (and O rescaled) when a block raises it by more than 2^8;
+// the probabilities are then at most 2^8, and the final O / l uses the same reference.
 //
 // Long prefixes with few (request, head, tile) triples are split over CTAs; each split writes
 // its unnormalised O with its running max and sum, and a combine kernel merges the splits.
@@ -32,7 +36,9 @@ namespace gdn {
 constexpr int kAttnRows = 128;      // query rows per tile (the MMA's M)
 constexpr int kAttnKeys = 128;      // prefix keys per block
 constexpr int kAttnTreeKeys = 64;   // the draft-node block (at most 64 nodes per request)
-constexpr int kAttnStages = 2;      // key/value blocks in flight
+constexpr int kAttnKStages = 3;     // key blocks in flight (a key block is free as soon as S is formed)
+constexpr int kAttnVStages = 3;     // value blocks in flight (free once P.V is done)
+constexpr float kAttnRescale = 8.f;  // log2 growth of a row's max that forces a rescale of O
 constexpr int kAttnThreads = 256;
 constexpr int kAttnSoftmaxWarp0 = 4;
 constexpr uint32_t kAttnTmemCols = 512;
@@ -49,20 +55,19 @@ struct AttnArgs {
   int32_t *status;
 };
 
-// Dynamic shared memory: Q, the K and V stages, P and alignment slack - and never less than
-// 120 KB, so that two CTAs (whose tensor-memory allocations would not both fit) never share an SM.
+// Dynamic shared memory: Q, the K and V stages (128 keys x 128 B per 64-column chunk) and
+// alignment slack - never less than 120 KB, so that two CTAs (whose tensor-memory allocations
+// would not both fit) never share an SM.
+__host__ __device__ constexpr uint32_t attn_smem_need(int D) {
+  return uint32_t(1 + kAttnKStages + kAttnVStages) * (D / 64) * 16384u + 1024u;
+}
 __host__ __device__ constexpr uint32_t attn_smem_bytes(int D) {
-  return (uint32_t(D / 64) * 16384u                    // Q: 128 rows x 128 B per 64-column chunk
-          + uint32_t(kAttnStages) * 2u * (D / 64) * 16384u  // K and V: 128 keys x 128 B per chunk
-          + 2u * 16384u                                  // P: 128 rows x 128 keys bf16
-          + 1024u) > 120u * 1024u
-             ? (uint32_t(D / 64) * 16384u + uint32_t(kAttnStages) * 2u * (D / 64) * 16384u + 2u * 16384u + 1024u)
-             : 120u * 1024u;
+  return attn_smem_need(D) > 120u * 1024u ? attn_smem_need(D) : 120u * 1024u;
 }
 
 struct AttnShared {
-  uint64_t q_full, k_full[kAttnStages], v_full[kAttnStages], kv_empty[kAttnStages];
-  uint64_t s_full[2], s_free[2], p_full, pv_done, drain;
+  uint64_t q_full, k_full[kAttnKStages], k_empty[kAttnKStages], v_full[kAttnVStages], v_empty[kAttnVStages];
+  uint64_t s_full[2], p_full, pv_done, o_final, drain;
   unsigned long long anc[64];
   uint32_t tmem_base;
   int abort_flag, go;
@@ -102,8 +107,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(attn_dyn_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *Qs = base;
   uint8_t *Ks = Qs + kQBytes;                        // [stage] K blocks
-  uint8_t *Vs = Ks + kAttnStages * kKVBytes;         // [stage] V blocks
-  uint8_t *Ps = Vs + kAttnStages * kKVBytes;         // P: 2 chunks of 64 keys
+  uint8_t *Vs = Ks + kAttnKStages * kKVBytes;        // [stage] V blocks
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x % a.splits, tile = blockIdx.x / a.splits;
@@ -159,17 +163,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (tid == 0) {
     ptx::mbar_init(&sh.q_full, 1);
-    for (int s = 0; s < kAttnStages; ++s) {
+    for (int s = 0; s < kAttnKStages; ++s) {
       ptx::mbar_init(&sh.k_full[s], 1);
+      ptx::mbar_init(&sh.k_empty[s], 1);
+    }
+    for (int s = 0; s < kAttnVStages; ++s) {
       ptx::mbar_init(&sh.v_full[s], 1);
-      ptx::mbar_init(&sh.kv_empty[s], 1);
+      ptx::mbar_init(&sh.v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&sh.s_full[b], 1);
-      ptx::mbar_init(&sh.s_free[b], 128);
-    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&sh.s_full[b], 1);
     ptx::mbar_init(&sh.p_full, 128);
     ptx::mbar_init(&sh.pv_done, 1);
+    ptx::mbar_init(&sh.o_final, 1);
     ptx::mbar_init(&sh.drain, 1);
     ptx::fence_mbar_init();
   }
@@ -183,93 +188,111 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = sh.tmem_base;
   const uint32_t O_col = 2 * kAttnKeys;  // S buffers at columns 0 and 128, O after them
 
-  uint32_t issued = 0;  // TMA thread: blocks whose copies were issued
-
-  if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+  if (warp == 0 || warp == 3) {
+    // ---------------------------------------------------------------- TMA producers
     if (lane == 0) {
-      ptx::prefetch_tensormap(&tm_q);
-      ptx::prefetch_tensormap(&tm_kc);
-      ptx::prefetch_tensormap(&tm_vc);
-      ptx::mbar_arrive_expect_tx(&sh.q_full, kQBytes);
+      const bool keys = warp == 0;
+      const int stages = keys ? kAttnKStages : kAttnVStages;
+      uint64_t *full = keys ? sh.k_full : sh.v_full;
+      uint64_t *empty = keys ? sh.k_empty : sh.v_empty;
+      uint8_t *buf = keys ? Ks : Vs;
+      const CUtensorMap *pre = keys ? &tm_kc : &tm_vc, *nodes = keys ? &tm_kt : &tm_vt;
+      ptx::prefetch_tensormap(pre);
+      if (keys) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::mbar_arrive_expect_tx(&sh.q_full, kQBytes);
 #pragma unroll
-      for (int c = 0; c < NCH; ++c)
-        ptx::tma_load_3d(Qs + c * kChunk, &tm_q, &sh.q_full, c * 64, g * G, t0 + t_begin);
+        for (int c = 0; c < NCH; ++c)
+          ptx::tma_load_3d(Qs + c * kChunk, &tm_q, &sh.q_full, c * 64, g * G, t0 + t_begin);
+      }
+      int issued = 0;
       for (int j = 0; j < nb; ++j) {
-        const int s = j % kAttnStages;
-        if (j >= kAttnStages && !attn_wait(&sh.kv_empty[s], ((j / kAttnStages) - 1) & 1, sh, a.status)) break;
+        const int st = j % stages;
+        if (j >= stages && !attn_wait(&empty[st], ((j / stages) - 1) & 1, sh, a.status)) break;
         const bool tree = j == nbp;
-        const uint32_t bytes = tree ? uint32_t(NCH) * kAttnTreeKeys * 128u : kKVBytes;
-        ptx::mbar_arrive_expect_tx(&sh.k_full[s], bytes);
+        ptx::mbar_arrive_expect_tx(&full[st], tree ? uint32_t(NCH) * kAttnTreeKeys * 128u : kKVBytes);
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
-          if (tree) ptx::tma_load_3d(Ks + s * kKVBytes + c * kChunk, &tm_kt, &sh.k_full[s], c * 64, g, t0);
-          else ptx::tma_load_3d(Ks + s * kKVBytes + c * kChunk, &tm_kc, &sh.k_full[s], c * 64, g,
+          if (tree) ptx::tma_load_3d(buf + st * kKVBytes + c * kChunk, nodes, &full[st], c * 64, g, t0);
+          else ptx::tma_load_3d(buf + st * kKVBytes + c * kChunk, pre, &full[st], c * 64, g,
                                 p0 + (b_lo + j) * kAttnKeys);
         }
-        ptx::mbar_arrive_expect_tx(&sh.v_full[s], bytes);
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          if (tree) ptx::tma_load_3d(Vs + s * kKVBytes + c * kChunk, &tm_vt, &sh.v_full[s], c * 64, g, t0);
-          else ptx::tma_load_3d(Vs + s * kKVBytes + c * kChunk, &tm_vc, &sh.v_full[s], c * 64, g,
-                                p0 + (b_lo + j) * kAttnKeys);
-        }
-        issued = uint32_t(j + 1);
+        issued = j + 1;
       }
       // clean-up: the copies of the last blocks issued have landed before the CTA exits
-      ptx::mbar_wait(&sh.q_full, 0, kAttnWaitNs);
-      for (int j = int(issued) - kAttnStages; j < int(issued); ++j) {
-        if (j < 0) continue;
-        ptx::mbar_wait(&sh.k_full[j % kAttnStages], (j / kAttnStages) & 1, kAttnWaitNs);
-        ptx::mbar_wait(&sh.v_full[j % kAttnStages], (j / kAttnStages) & 1, kAttnWaitNs);
-      }
+      if (keys) ptx::mbar_wait(&sh.q_full, 0, kAttnWaitNs);
+      for (int j = issued - stages; j < issued; ++j)
+        if (j >= 0) ptx::mbar_wait(&full[j % stages], (j / stages) & 1, kAttnWaitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = ptx::smem_u32(Qs), p_addr = ptx::smem_u32(Ps);
+      const uint32_t q_addr = ptx::smem_u32(Qs);
       bool ok = attn_wait(&sh.q_full, 0, sh, a.status);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kAttnStages;
-        if (!attn_wait(&sh.k_full[s], (j / kAttnStages) & 1, sh, a.status)) return false;
-        if (j >= 2 && !attn_wait(&sh.s_free[j & 1], ((j >> 1) - 1) & 1, sh, a.status)) return false;
-        ptx::tc_fence_after_sync();
-        const bool tree = j == nbp;
-        const uint32_t idesc = ptx::idesc_bf16_f32(kAttnRows, tree ? kAttnTreeKeys : kAttnKeys);
-        const uint32_t k_addr = ptx::smem_u32(Ks + s * kKVBytes);
+      // polls both streams: S_j needs its key block and a free S buffer - block j - 2's P.V, which
+      // reads its probabilities from that buffer, issued before it (one thread's MMAs run in
+      // order); P.V_j needs block j's probabilities and its value block
+      int si = 0, pi = 0;
+      uint32_t idle = 0;
+      uint64_t idle_since = 0;
+      while (ok && pi < nb) {
+        bool progress = false;
+        if (si < nb) {
+          const int sk = si % kAttnKStages;
+          if (si <= pi + 1 && ptx::mbar_test_wait(&sh.k_full[sk], (si / kAttnKStages) & 1)) {
+            ptx::tc_fence_after_sync();
+            const bool tree = si == nbp;
+            const uint32_t idesc = ptx::idesc_bf16_f32(kAttnRows, tree ? kAttnTreeKeys : kAttnKeys);
+            const uint32_t k_addr = ptx::smem_u32(Ks + sk * kKVBytes);
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
+            for (int c = 0; c < NCH; ++c)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::mma_bf16_ss(tmem + uint32_t(j & 1) * kAttnKeys,
-                             ptx::desc_kmajor_sw128(q_addr + c * kChunk + kk * 32),
-                             ptx::desc_kmajor_sw128(k_addr + c * kChunk + kk * 32), idesc, (c | kk) != 0);
-        ptx::mma_commit(&sh.s_full[j & 1]);
-        return true;
-      };
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j % kAttnStages;
-        if (!attn_wait(&sh.p_full, j & 1, sh, a.status)) return false;
-        if (!attn_wait(&sh.v_full[s], (j / kAttnStages) & 1, sh, a.status)) return false;
-        ptx::tc_fence_after_sync();
-        const int ksteps = (j == nbp ? kAttnTreeKeys : kAttnKeys) / 16;
-        const uint32_t idesc = ptx::idesc_bf16_f32_bmn(kAttnRows, 64);
-        const uint32_t v_addr = ptx::smem_u32(Vs + s * kKVBytes);
-        for (int ks = 0; ks < ksteps; ++ks)
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_bf16_ss(tmem + uint32_t(si & 1) * kAttnKeys,
+                                 ptx::desc_kmajor_sw128(q_addr + c * kChunk + kk * 32),
+                                 ptx::desc_kmajor_sw128(k_addr + c * kChunk + kk * 32), idesc, (c | kk) != 0);
+            ptx::mma_commit(&sh.s_full[si & 1]);
+            ptx::mma_commit(&sh.k_empty[sk]);
+            ++si;
+            progress = true;
+          }
+        }
+        if (pi < si) {
+          const int sv = pi % kAttnVStages;
+          if (ptx::mbar_test_wait(&sh.p_full, pi & 1) &&
+              ptx::mbar_test_wait(&sh.v_full[sv], (pi / kAttnVStages) & 1)) {
+            ptx::tc_fence_after_sync();
+            const int ksteps = (pi == nbp ? kAttnTreeKeys : kAttnKeys) / 16;
+            const uint32_t idesc = ptx::idesc_bf16_f32_bmn(kAttnRows, 64);
+            const uint32_t v_addr = ptx::smem_u32(Vs + sv * kKVBytes);
+            const uint32_t p_tmem = tmem + uint32_t(pi & 1) * kAttnKeys;  // 16 keys = 8 packed columns
+            for (int ks = 0; ks < ksteps; ++ks)
 #pragma unroll
-          for (int c = 0; c < NCH; ++c)
-            ptx::mma_bf16_ss(tmem + O_col + uint32_t(c * 64),
-                             ptx::desc_kmajor_sw128(p_addr + (ks >> 2) * kChunk + (ks & 3) * 32),
-                             ptx::desc_mnmajor_sw128(v_addr + c * kChunk + ks * 2048), idesc, (j | ks) != 0);
-        ptx::mma_commit(&sh.pv_done);
-        ptx::mma_commit(&sh.kv_empty[s]);
-        return true;
-      };
-      if (ok && nb > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < nb; ++j) {
-        if (j + 1 < nb && !issue_s(j + 1)) break;
-        if (!issue_pv(j)) break;
+              for (int c = 0; c < NCH; ++c)
+                ptx::mma_bf16_ts(tmem + O_col + uint32_t(c * 64), p_tmem + uint32_t(ks * 8),
+                                 ptx::desc_mnmajor_sw128(v_addr + c * kChunk + ks * 2048), idesc, (pi | ks) != 0);
+            ptx::mma_commit(&sh.pv_done);
+            ptx::mma_commit(&sh.v_empty[sv]);
+            ++pi;
+            progress = true;
+          }
+        }
+        if (progress) {
+          idle = 0;
+        } else if ((++idle & 63u) == 0) {  // bounded: give up after the wait limit without progress
+          if (*reinterpret_cast<volatile int *>(&sh.abort_flag)) break;
+          const uint64_t now = ptx::globaltimer_ns();
+          if (idle == 64) idle_since = now;
+          else if (now - idle_since > kAttnWaitNs) {
+            *reinterpret_cast<volatile int *>(&sh.abort_flag) = 1;
+            report(a.status, GDN_STATUS_TIMEOUT);
+            break;
+          }
+        }
       }
+      // O is final once every P.V has completed (the epilogue waits on this single phase: the
+      // per-block barrier may trail the last block by two phases, which a parity wait cannot tell)
+      if (pi == nb && nb > 0) ptx::mma_commit(&sh.o_final);
       // clean-up: every MMA this thread issued has completed
       ptx::mma_commit(&sh.drain);
       ptx::mbar_wait(&sh.drain, 0, kAttnWaitNs);
@@ -292,42 +315,54 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       ptx::tc_fence_after_sync();
-      float sc[kAttnKeys];
+      // mask: only a partial prefix block and the draft-node block need one
+      const int key0 = (b_lo + j) * kAttnKeys;
+      const int lim = tree ? 0 : P - key0;  // visible prefix keys of this block
+      const bool full = row_ok && !tree && lim >= kAttnKeys;
+      // draft-node block: key c is visible iff bit c of the row's ancestor mask is set (n <= 64 keys)
+      const unsigned long long vis_tree = row_ok ? anc_t : 0ull;
+      auto masked = [&](float (&x)[64], int c0) {
+        if (full) return;
+        if (!row_ok) {
 #pragma unroll
-      for (int c = 0; c < kAttnKeys; ++c) sc[c] = 0.f;
+          for (int e = 0; e < 64; ++e) x[e] = -INFINITY;
+        } else if (tree) {  // c0 == 0: the block has 64 keys
+          const uint32_t lo = uint32_t(vis_tree), hi = uint32_t(vis_tree >> 32);
 #pragma unroll
-      for (int c0 = 0; c0 < kAttnKeys; c0 += 16) {
+          for (int e = 0; e < 64; ++e)
+            if (!(((e < 32 ? lo : hi) >> (e & 31)) & 1u)) x[e] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (c0 + e >= lim) x[e] = -INFINITY;
+        }
+      };
+      const uint32_t s_addr = tmem + lane_addr + uint32_t(j & 1) * kAttnKeys;
+      // pass 1: block max of the raw scores (the scale is positive: the scaled max is the max scaled)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c0 = 0; c0 < kAttnKeys; c0 += 64) {
         if (c0 < ncols) {
-          float x[16];
-          ptx::tmem_ld_32x32b_x16(tmem + lane_addr + uint32_t(j & 1) * kAttnKeys + uint32_t(c0), x);
+          float x[64];
+          ptx::tmem_ld_32x32b_x64(s_addr + uint32_t(c0), x);
+          masked(x, c0);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) sc[c0 + e] = x[e];
+          for (int e = 0; e < 64; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
         }
       }
-      ptx::tc_fence_before_sync();
-      attn_arrive(&sh.s_free[j & 1]);
-      // mask, scale (log2 domain), block max
-      const int key0 = (b_lo + j) * kAttnKeys;
-      float bmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kAttnKeys; ++c) {
-        bool vis;
-        if (tree) vis = c < kAttnTreeKeys && c < n && ((anc_t >> (c & 63)) & 1ull);
-        else vis = key0 + c < P;
-        vis = vis && row_ok;
-        sc[c] = vis ? sc[c] * a.scale_log2 : -INFINITY;
-        bmax = fmaxf(bmax, sc[c]);
-      }
-      const float m_new = fmaxf(m, bmax);
-      const float alpha = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+      const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+      const float m_new = bmax > m + kAttnRescale ? bmax : m;  // the reference max moves only by > 2^8
+      const float alpha = m_new == m ? 1.f : exp2f(m - m_new);
       const float m_sub = m_new == -INFINITY ? 0.f : m_new;  // a row with no visible key yet: every p is 0
-      // the previous block's P.V has finished: P may be overwritten, O is stable
-      if (j > 0 && !attn_wait(&sh.pv_done, (j - 1) & 1, sh, a.status)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after_sync();
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale this warp's O rows
+        // O is stable once the previous block's P.V has finished. S_j was issued after P.V_{j-2}
+        // and its commit covers it, so the P.V barrier is at phase j - 1 (pending) or past it:
+        // the parity wait is unambiguous
+        if (!attn_wait(&sh.pv_done, (j - 1) & 1, sh, a.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           float x[16];
@@ -337,36 +372,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ptx::tmem_st_32x32b_x16(tmem + lane_addr + O_col + uint32_t(c0), x);
         }
       }
-      // probabilities, rounded to bf16 as the P.V product sees them (their sum uses the same
-      // rounded values), written as row i of P: K-major with the 128-byte swizzle, 16-byte unit u
-      // of the row at position u ^ (i & 7)
-      float psum = 0.f;
+      // pass 2: probabilities p = 2^(scale s - m), rounded to bf16 and written back over this S
+      // buffer as row i of P, two keys per 32-bit column (keys 0..63 into columns 0..31, whose
+      // scores pass 2 has already read, and so on). Their sum is taken before rounding (each
+      // rounded weight is within 2^-8 of its exact value, the same bound as rounding the sum).
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      const float sl = a.scale_log2;
 #pragma unroll
       for (int ch = 0; ch < kAttnKeys / 64; ++ch) {
         if (ch * 64 < ncols) {
-          uint8_t *row = Ps + ch * kChunk + (i >> 3) * 1024 + (i & 7) * 128;
+          float x[64];
+          ptx::tmem_ld_32x32b_x64(s_addr + uint32_t(ch * 64), x);
+          masked(x, ch * 64);
+          uint32_t w[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = ch * 64 + u * 8 + 2 * e;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(exp2f(sc[c] - m_sub), exp2f(sc[c + 1] - m_sub));
-              psum += __low2float(b2) + __high2float(b2);
-              w[e] = *reinterpret_cast<const uint32_t *>(&b2);
-            }
-            *reinterpret_cast<uint4 *>(row + ((u ^ (i & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 32; ++e) {
+            const float e0 = ptx::ex2_approx(fmaf(x[2 * e], sl, -m_sub));
+            const float e1 = ptx::ex2_approx(fmaf(x[2 * e + 1], sl, -m_sub));
+            ps[e & 3] += e0 + e1;
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
+            w[e] = *reinterpret_cast<const uint32_t *>(&b2);
           }
+          ptx::tmem_st_32x32b_x32(s_addr + uint32_t(ch * 32), w);
         }
       }
-      l = l * alpha + psum;
+      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       m = m_new;
-      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before_sync();
       attn_arrive(&sh.p_full);
     }
     // epilogue: the last P.V has finished
-    if (ok && nb > 0 && attn_wait(&sh.pv_done, (nb - 1) & 1, sh, a.status)) {
+    if (ok && nb > 0 && attn_wait(&sh.o_final, 0, sh, a.status)) {
       ptx::tc_fence_after_sync();
       const int h = g * G + hq;
       float *dst;

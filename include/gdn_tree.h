@@ -356,7 +356,7 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
  *   cu_prefix [B+1], parent [T], cu_nodes [B+1] int32 in   as for gdn_tree_verify; at most
  *                                          max_nodes (<= 64) nodes and max_prefix keys per request
  *   d                                 64 or 128; H_q / H_kv a power of two <= 128
- *   scale                             score scale (e.g. d^-1/2)
+ *   scale                             score scale, > 0 (e.g. d^-1/2)
  *   o        [T][H_q][d]        fp32  out  written for every node of every valid request
  *   workspace, workspace_bytes        optional device scratch: with too few (request, head)
  *                                     pairs to fill the GPU, long prefixes are split across CTAs

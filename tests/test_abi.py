@@ -163,7 +163,8 @@ def test_grow_host_checks(kw, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(Hq=12, Hkv=4), gb.GDN_EINVAL),  # group of 3 query heads: not a power of two
     (dict(Hq=6, Hkv=4), gb.GDN_EINVAL), (dict(d=32), gb.GDN_EINVAL), (dict(max_nodes=65), gb.GDN_ETOOBIG),
-    (dict(scale=float("inf")), gb.GDN_EINVAL), (dict(q=None), gb.GDN_EINVAL), (dict(kc=None), gb.GDN_EINVAL),
+    (dict(scale=float("inf")), gb.GDN_EINVAL), (dict(scale=0.0), gb.GDN_EINVAL), (dict(scale=-0.5), gb.GDN_EINVAL),
+    (dict(q=None), gb.GDN_EINVAL), (dict(kc=None), gb.GDN_EINVAL),
     (dict(o=FAKE + 4), gb.GDN_EALIGN), (dict(B=0), gb.GDN_OK), (dict(max_nodes=0), gb.GDN_OK),
     (dict(kc=None, vc=None, P=0), gb.GDN_ECUDA)])  # valid arguments: only the missing GPU stops it
 def test_attention_host_checks(kw, code):
