@@ -63,6 +63,7 @@ _SIGS = {
     "gdn_tree_budget_topb": [_P] + [_I] * 3 + [_P] * 5 + [_P],
     "gdn_tree_grow_best_first": [_P] + [_I] * 3 + [ctypes.c_float, _I] + [_P] * 7 + [_P],
     "gdn_tree_attention": [_P] * 8 + [_I] * 8 + [ctypes.c_float, _P, _P, ctypes.c_size_t, _P, _P],
+    "gdn_tree_attention_noalloc": [_P] * 8 + [_I] * 8 + [ctypes.c_float, _P, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -237,3 +238,11 @@ def gdn_tree_attention(q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, B
                                    _ptr(parent), _ptr(cu_nodes), B, H_q, H_kv, T, P_total, d, max_nodes, max_prefix,
                                    float(scale), _ptr(o), _ptr(workspace), int(workspace_bytes), _ptr(status),
                                    _stream(stream)), "gdn_tree_attention")
+
+
+def gdn_tree_attention_noalloc(q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, B, H_q, H_kv, T, P_total, d,
+                               max_nodes, max_prefix, scale, o, status=None, stream=None):
+    _check(_lib.gdn_tree_attention_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(cu_prefix),
+                                           _ptr(parent), _ptr(cu_nodes), B, H_q, H_kv, T, P_total, d, max_nodes,
+                                           max_prefix, float(scale), _ptr(o), _ptr(status), _stream(stream)),
+           "gdn_tree_attention_noalloc")

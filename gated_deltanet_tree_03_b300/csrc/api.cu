@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/gdn_tree.h: argument checks, launch
 // configuration, TMA descriptor encoding and kernel dispatch. Nothing here allocates device
-// memory, synchronises the device or keeps per-call state.
+// memory, synchronises the device or keeps per-call state; the one fixed buffer is the scratch
+// array of gdn_tree_attention_noalloc (with its per-device address, looked up once).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -447,6 +448,39 @@ gdn_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t
 
 }  // namespace
 
+// Scratch of gdn_tree_attention_noalloc: the split partial outputs and (max, sum) pairs, in a
+// fixed array of the module rather than a caller buffer. Every GPU that loads the library holds
+// these 32 MiB until the process exits; every call of that entry point shares them.
+constexpr size_t kAttnNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kAttnNoAllocScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+// The device address of the scratch array on the current device, looked up once per device.
+// (Host code cannot use the array's name as a device pointer.)
+gdn_status noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      fprintf(stderr, "gdn_tree: scratch address lookup failed: %s\n", cudaGetErrorString(e));
+      return GDN_ECUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t gdn_abi_version(void) { return 3; }
@@ -654,6 +688,31 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
   if ((st = launch_status()) != GDN_OK) return st;
   pack_copy_kernel<<<unsigned((R + kCopyWarps - 1) / kCopyWarps), kCopyWarps * 32, 0, s>>>(pa);
   return launch_status();
+}
+
+gdn_status gdn_tree_attention_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                      const uint16_t *k_cache, const uint16_t *v_cache, const int32_t *cu_prefix,
+                                      const int32_t *parent, const int32_t *cu_nodes, int32_t B, int32_t H_q,
+                                      int32_t H_kv, int32_t T, int32_t P_total, int32_t d, int32_t max_nodes,
+                                      int32_t max_prefix, float scale, float *o, int32_t *status, gdn_stream_t stream) {
+  gdn_status st = check_attn_shape(B, H_q, H_kv, d, max_nodes, max_prefix);
+  if (st != GDN_OK) return st;
+  if (B == 0 || T == 0 || max_nodes == 0) return GDN_OK;
+  // the same key splits gdn_tree_attention plans with an unlimited workspace; refuse what does not fit
+  const size_t need = attn_plan(B, H_q, H_kv, d, max_nodes, max_prefix, ~size_t(0)).ws_bytes;
+  if (need > kAttnNoAllocScratchBytes) {
+    fprintf(stderr, "gdn_tree_attention_noalloc: these sizes need %zu bytes of scratch, more than the built-in %zu\n",
+            need, kAttnNoAllocScratchBytes);
+    return GDN_ETOOBIG;
+  }
+  if (T < 0 || P_total < 0 || !std::isfinite(scale) || !(scale > 0.f)) return GDN_EINVAL;
+  void *scratch = nullptr;
+  if (need > 0) {
+    if ((st = check_device()) != GDN_OK) return st;
+    if ((st = noalloc_scratch(&scratch)) != GDN_OK) return st;
+  }
+  return gdn_tree_attention(q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, B, H_q, H_kv, T, P_total, d,
+                            max_nodes, max_prefix, scale, o, scratch, need, status, stream);
 }
 
 size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t max_nodes,

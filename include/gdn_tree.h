@@ -381,6 +381,31 @@ gdn_status gdn_tree_attention(const uint16_t *q, const uint16_t *k, const uint16
 size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t d,
                                          int32_t max_nodes, int32_t max_prefix);
 
+/*
+ * gdn_tree_attention_noalloc - gdn_tree_attention for callers that cannot allocate device
+ * memory: a serving engine whose allocator reserved the GPU's memory at start-up for its KV-cache
+ * pool, or a host framework that forbids allocation inside a forward step, has no buffer to
+ * offer as workspace. The pages have no counterpart of this entry point; it only moves the
+ * workspace of the key splits into scratch the library owns.
+ *
+ * Same arguments and results as gdn_tree_attention, without workspace and workspace_bytes. It
+ * makes the key splits gdn_tree_attention would make with gdn_tree_attention_workspace_size()
+ * bytes of workspace, in a 32 MiB scratch array built into the library: every GPU that loads
+ * the library holds those 32 MiB until the process exits. Sizes that need more scratch return
+ * GDN_ETOOBIG (with a message on stderr) before anything is launched. It calls no allocator.
+ * The first call that needs scratch on a device looks up the array's device address for that
+ * device (make that first call before any stream capture). Every call shares the one array and
+ * writes the parts it reads, so nothing needs clearing between calls, but two calls that overlap
+ * on the GPU (other streams, other host threads) race on it.
+ */
+gdn_status gdn_tree_attention_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                      const uint16_t *k_cache, const uint16_t *v_cache,
+                                      const int32_t *cu_prefix, const int32_t *parent,
+                                      const int32_t *cu_nodes, int32_t B, int32_t H_q, int32_t H_kv,
+                                      int32_t T, int32_t P_total, int32_t d, int32_t max_nodes,
+                                      int32_t max_prefix, float scale, float *o, int32_t *status,
+                                      gdn_stream_t stream);
+
 /* Human-readable name of a return code (static string, never NULL). */
 const char *gdn_status_str(gdn_status s);
 

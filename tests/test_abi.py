@@ -11,7 +11,7 @@ EXPECTED = {"gdn_tree_verify", "gdn_tree_verify_simt", "gdn_tree_commit", "gdn_t
             "gdn_tree_commit_storeall", "gdn_tree_accept_greedy", "gdn_tree_commit_verify", "gdn_status_str",
             "gdn_abi_version", "gdn_tree_verify_ex", "gdn_tree_commit_ex", "gdn_tree_commit_verify_ex",
             "gdn_tree_budget_topb", "gdn_tree_grow_best_first", "gdn_tree_attention",
-            "gdn_tree_attention_workspace_size"}
+            "gdn_tree_attention_workspace_size", "gdn_tree_attention_noalloc"}
 
 
 def test_header_declares_expected_symbols():
