@@ -185,3 +185,17 @@ def test_attention_workspace_size_is_zero_without_splits():
     assert gb.gdn_tree_attention_workspace_size(4, 16, 2, 128, 8, 100) == 0  # one key block: nothing to split
     big = gb.gdn_tree_attention_workspace_size(1, 16, 2, 128, 6, 8192)
     assert big > 0 and big % (128 * 130 * 4) == 0
+
+
+def test_attention_workspace_stays_under_its_bound():
+    """The key splits aim at two CTAs per SM, so the workspace stays under 4 x SMs x 128 rows x
+    (d + 2) floats: with the host's SM count unknown here, the planner assumes 148 SMs."""
+    bound = lambda d: 4 * 148 * 128 * (d + 2) * 4
+    for B in (1, 2, 5, 17, 64, 150, 300):
+        for Hq, Hkv in ((16, 2), (8, 8), (32, 4), (4, 1)):
+            for d in (64, 128):
+                for mn in (1, 6, 32, 64):
+                    for mp in (0, 100, 4096, 40000):
+                        ws = gb.gdn_tree_attention_workspace_size(B, Hq, Hkv, d, mn, mp)
+                        assert ws <= bound(d), (B, Hq, Hkv, d, mn, mp, ws)
+                        assert ws % (128 * (d + 2) * 4) == 0
