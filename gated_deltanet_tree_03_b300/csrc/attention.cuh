@@ -16,7 +16,10 @@
 //     O += P V         tcgen05.mma with P read from tensor memory and V read as an MN-major
 //                      operand straight from its TMA tile
 // Warp roles: 0 key (and query) TMA producer, 1 MMA issuer (issues whichever of the next S and
-// the next P.V is ready), 2 tree masks, 3 value TMA producer, 4..7 softmax and epilogue.
+// the next P.V is ready), 2 tree masks, 3 value TMA producer, 4..11 softmax and epilogue in two
+// warpgroups: warps 4..7 take key columns 0..63 of every block, warps 8..11 columns 64..127,
+// each half with its own running max and sum and its own O accumulator in tensor memory; the
+// two halves are merged once, in the epilogue.
 // A row's running max is only moved (and O rescaled) when a block raises it by more than 2^8;
 // the probabilities are then at most 2^8, and the final O / l uses the same reference.
 //
@@ -39,7 +42,7 @@ constexpr int kAttnTreeKeys = 64;   // the draft-node block (at most 64 nodes pe
 constexpr int kAttnKStages = 3;     // key blocks in flight (a key block is free as soon as S is formed)
 constexpr int kAttnVStages = 3;     // value blocks in flight (free once P.V is done)
 constexpr float kAttnRescale = 8.f;  // log2 growth of a row's max that forces a rescale of O
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 384;
 constexpr int kAttnSoftmaxWarp0 = 4;
 constexpr uint32_t kAttnTmemCols = 512;
 constexpr uint64_t kAttnWaitNs = 1000000000ull;  // 1 s bound on every wait
@@ -67,11 +70,18 @@ __host__ __device__ constexpr uint32_t attn_smem_bytes(int D) {
 
 struct AttnShared {
   uint64_t q_full, k_full[kAttnKStages], k_empty[kAttnKStages], v_full[kAttnVStages], v_empty[kAttnVStages];
-  uint64_t s_full[2], p_full, pv_done, o_final, drain;
+  // p_full[b]: every softmax thread has written block j's P, for blocks j with j & 1 == b. Two of
+  // them, so that a thread already on block j + 1 cannot complete block j's phase: it can reach
+  // block j + 2 (the same barrier) only after block j's P.V was issued.
+  uint64_t s_full[2], p_full[2], pv_done, o_final, drain;
   unsigned long long anc[64];
   uint32_t tmem_base;
   int abort_flag, go;
 };
+
+__device__ __forceinline__ void attn_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ __forceinline__ bool attn_wait(uint64_t *bar, uint32_t parity, AttnShared &sh, int32_t *status) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -172,7 +182,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       ptx::mbar_init(&sh.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(&sh.s_full[b], 1);
-    ptx::mbar_init(&sh.p_full, 128);
+    ptx::mbar_init(&sh.p_full[0], 256);
+    ptx::mbar_init(&sh.p_full[1], 256);
     ptx::mbar_init(&sh.pv_done, 1);
     ptx::mbar_init(&sh.o_final, 1);
     ptx::mbar_init(&sh.drain, 1);
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
-  const uint32_t O_col = 2 * kAttnKeys;  // S buffers at columns 0 and 128, O after them
+  const uint32_t O_col = 2 * kAttnKeys;  // S buffers at columns 0 and 128, then O of half 0, O of half 1
 
   if (warp == 0 || warp == 3) {
     // ---------------------------------------------------------------- TMA producers
@@ -233,6 +244,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // reads its probabilities from that buffer, issued before it (one thread's MMAs run in
       // order); P.V_j needs block j's probabilities and its value block
       int si = 0, pi = 0;
+      bool o1_started = false;  // half 1's O has had its first (overwriting) P.V
       uint32_t idle = 0;
       uint64_t idle_since = 0;
       while (ok && pi < nb) {
@@ -259,18 +271,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         if (pi < si) {
           const int sv = pi % kAttnVStages;
-          if (ptx::mbar_test_wait(&sh.p_full, pi & 1) &&
+          if (ptx::mbar_test_wait(&sh.p_full[pi & 1], (pi >> 1) & 1) &&
               ptx::mbar_test_wait(&sh.v_full[sv], (pi / kAttnVStages) & 1)) {
             ptx::tc_fence_after_sync();
-            const int ksteps = (pi == nbp ? kAttnTreeKeys : kAttnKeys) / 16;
             const uint32_t idesc = ptx::idesc_bf16_f32_bmn(kAttnRows, 64);
             const uint32_t v_addr = ptx::smem_u32(Vs + sv * kKVBytes);
-            const uint32_t p_tmem = tmem + uint32_t(pi & 1) * kAttnKeys;  // 16 keys = 8 packed columns
-            for (int ks = 0; ks < ksteps; ++ks)
+            const uint32_t p_tmem = tmem + uint32_t(pi & 1) * kAttnKeys;
+            // half h: keys 64 h .. 64 h + 63, whose P that half wrote (packed, 16 keys = 8 columns)
+            // at columns 64 h .. 64 h + 31 of the buffer, into O of half h; the draft-node block
+            // has keys for half 0 only
+            const int halves = pi == nbp ? 1 : 2;
+            for (int h2 = 0; h2 < halves; ++h2) {
+              for (int kq = 0; kq < 4; ++kq) {
+                const int ks = h2 * 4 + kq;
+                const uint32_t acc = h2 == 0 ? uint32_t((pi | kq) != 0) : uint32_t(o1_started || kq != 0);
 #pragma unroll
-              for (int c = 0; c < NCH; ++c)
-                ptx::mma_bf16_ts(tmem + O_col + uint32_t(c * 64), p_tmem + uint32_t(ks * 8),
-                                 ptx::desc_mnmajor_sw128(v_addr + c * kChunk + ks * 2048), idesc, (pi | ks) != 0);
+                for (int c = 0; c < NCH; ++c)
+                  ptx::mma_bf16_ts(tmem + O_col + uint32_t(h2 * D + c * 64), p_tmem + uint32_t(h2 * 64 + kq * 8),
+                                   ptx::desc_mnmajor_sw128(v_addr + c * kChunk + ks * 2048), idesc, acc);
+              }
+              if (h2 == 1) o1_started = true;
+            }
             ptx::mma_commit(&sh.pv_done);
             ptx::mma_commit(&sh.v_empty[sv]);
             ++pi;
@@ -299,91 +320,85 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp >= kAttnSoftmaxWarp0) {
     // ---------------------------------------------------------------- softmax and epilogue
-    const int i = tid - kAttnSoftmaxWarp0 * 32;  // query row = TMEM lane
+    const int hf = (warp - kAttnSoftmaxWarp0) / 4;           // key half of this warpgroup
+    const int i = ((warp - kAttnSoftmaxWarp0) & 3) * 32 + lane;  // query row = TMEM lane
     const int t_local = i / G, hq = i % G;
     const int t = t_begin + t_local;
     const bool row_ok = t < n;
     const unsigned long long anc_t = row_ok ? sh.anc[t] : 0ull;
-    const uint32_t lane_addr = uint32_t((warp - kAttnSoftmaxWarp0) * 32) << 16;
+    const uint32_t lane_addr = uint32_t(((warp - kAttnSoftmaxWarp0) & 3) * 32) << 16;
+    const uint32_t o_addr = tmem + lane_addr + O_col + uint32_t(hf * D);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; ok && j < nb; ++j) {
       const bool tree = j == nbp;
-      const int ncols = tree ? kAttnTreeKeys : kAttnKeys;
       if (!attn_wait(&sh.s_full[j & 1], (j >> 1) & 1, sh, a.status)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after_sync();
-      // mask: only a partial prefix block and the draft-node block need one
-      const int key0 = (b_lo + j) * kAttnKeys;
-      const int lim = tree ? 0 : P - key0;  // visible prefix keys of this block
-      const bool full = row_ok && !tree && lim >= kAttnKeys;
-      // draft-node block: key c is visible iff bit c of the row's ancestor mask is set (n <= 64 keys)
-      const unsigned long long vis_tree = row_ok ? anc_t : 0ull;
-      auto masked = [&](float (&x)[64], int c0) {
-        if (full) return;
-        if (!row_ok) {
+      if (!tree || hf == 0) {  // the draft-node block's <= 64 keys are all in half 0
+        // mask: only a partial prefix block and the draft-node block need one
+        const int lim = tree ? 0 : P - (b_lo + j) * kAttnKeys - hf * 64;  // visible prefix keys of this half
+        const bool full = row_ok && !tree && lim >= 64;
+        auto masked = [&](float (&x)[64]) {
+          if (full) return;
+          if (!row_ok) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) x[e] = -INFINITY;
-        } else if (tree) {  // c0 == 0: the block has 64 keys
-          const uint32_t lo = uint32_t(vis_tree), hi = uint32_t(vis_tree >> 32);
+            for (int e = 0; e < 64; ++e) x[e] = -INFINITY;
+          } else if (tree) {  // key e is visible iff bit e of the row's ancestor mask is set
+            const uint32_t lo = uint32_t(anc_t), hi = uint32_t(anc_t >> 32);
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (!(((e < 32 ? lo : hi) >> (e & 31)) & 1u)) x[e] = -INFINITY;
-        } else {
+            for (int e = 0; e < 64; ++e)
+              if (!(((e < 32 ? lo : hi) >> (e & 31)) & 1u)) x[e] = -INFINITY;
+          } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (c0 + e >= lim) x[e] = -INFINITY;
-        }
-      };
-      const uint32_t s_addr = tmem + lane_addr + uint32_t(j & 1) * kAttnKeys;
-      // pass 1: block max of the raw scores (the scale is positive: the scaled max is the max scaled)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c0 = 0; c0 < kAttnKeys; c0 += 64) {
-        if (c0 < ncols) {
+            for (int e = 0; e < 64; ++e)
+              if (e >= lim) x[e] = -INFINITY;
+          }
+        };
+        const uint32_t s_addr = tmem + lane_addr + uint32_t(j & 1) * kAttnKeys + uint32_t(hf * 64);
+        // pass 1: block max of the raw scores (the scale is positive: the scaled max is the max scaled)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        {
           float x[64];
-          ptx::tmem_ld_32x32b_x64(s_addr + uint32_t(c0), x);
-          masked(x, c0);
+          ptx::tmem_ld_32x32b_x64(s_addr, x);
+          masked(x);
 #pragma unroll
           for (int e = 0; e < 64; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
         }
-      }
-      const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-      const float m_new = bmax > m + kAttnRescale ? bmax : m;  // the reference max moves only by > 2^8
-      const float alpha = m_new == m ? 1.f : exp2f(m - m_new);
-      const float m_sub = m_new == -INFINITY ? 0.f : m_new;  // a row with no visible key yet: every p is 0
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale this warp's O rows
-        // O is stable once the previous block's P.V has finished. S_j was issued after P.V_{j-2}
-        // and its commit covers it, so the P.V barrier is at phase j - 1 (pending) or past it:
-        // the parity wait is unambiguous
-        if (!attn_wait(&sh.pv_done, (j - 1) & 1, sh, a.status)) {
-          ok = false;
-          break;
+        const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+        const float m_new = bmax > m + kAttnRescale ? bmax : m;  // the reference max moves only by > 2^8
+        const float alpha = m_new == m ? 1.f : exp2f(m - m_new);
+        const float m_sub = m_new == -INFINITY ? 0.f : m_new;  // a row with no visible key yet: every p is 0
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // rescale this warp's O rows of this half
+          // O is stable once the previous block's P.V has finished. S_j was issued after
+          // P.V_{j-2} and its commit covers it, so the P.V barrier is at phase j - 1 (pending)
+          // or past it: the parity wait is unambiguous
+          if (!attn_wait(&sh.pv_done, (j - 1) & 1, sh, a.status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            float x[16];
+            ptx::tmem_ld_32x32b_x16(o_addr + uint32_t(c0), x);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] *= alpha;
+            ptx::tmem_st_32x32b_x16(o_addr + uint32_t(c0), x);
+          }
         }
-        ptx::tc_fence_after_sync();
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          float x[16];
-          ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(c0), x);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] *= alpha;
-          ptx::tmem_st_32x32b_x16(tmem + lane_addr + O_col + uint32_t(c0), x);
-        }
-      }
-      // pass 2: probabilities p = 2^(scale s - m), rounded to bf16 and written back over this S
-      // buffer as row i of P, two keys per 32-bit column (keys 0..63 into columns 0..31, whose
-      // scores pass 2 has already read, and so on). Their sum is taken before rounding (each
-      // rounded weight is within 2^-8 of its exact value, the same bound as rounding the sum).
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      const float sl = a.scale_log2;
-#pragma unroll
-      for (int ch = 0; ch < kAttnKeys / 64; ++ch) {
-        if (ch * 64 < ncols) {
+        // pass 2: probabilities p = 2^(scale s - m), rounded to bf16 and written back over the
+        // first 32 columns of this half's scores (already read), two keys per 32-bit column.
+        // Their sum is taken before rounding (each rounded weight is within 2^-8 of its exact
+        // value, the same bound as rounding the sum).
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        const float sl = a.scale_log2;
+        {
           float x[64];
-          ptx::tmem_ld_32x32b_x64(s_addr + uint32_t(ch * 64), x);
-          masked(x, ch * 64);
+          ptx::tmem_ld_32x32b_x64(s_addr, x);
+          masked(x);
           uint32_t w[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
@@ -393,43 +408,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
             w[e] = *reinterpret_cast<const uint32_t *>(&b2);
           }
-          ptx::tmem_st_32x32b_x32(s_addr + uint32_t(ch * 32), w);
+          ptx::tmem_st_32x32b_x32(s_addr, w);
         }
+        l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+        m = m_new;
       }
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      m = m_new;
       ptx::tc_fence_before_sync();
-      attn_arrive(&sh.p_full);
+      attn_arrive(&sh.p_full[j & 1]);
     }
-    // epilogue: the last P.V has finished
-    if (ok && nb > 0 && attn_wait(&sh.o_final, 0, sh, a.status)) {
+    // epilogue: the last P.V has finished; merge the halves, O = (w0 O_0 + w1 O_1) / (w0 l_0 + w1 l_1)
+    // with w_h = 2^(m_h - M), M the larger max
+    const bool fin = ok && nb > 0 && attn_wait(&sh.o_final, 0, sh, a.status);
+    // each half's running max and sum per row, exchanged through the query buffer: every MMA
+    // (the only reader of Q) has completed once O is final
+    float (*ml)[kAttnRows][2] = reinterpret_cast<float (*)[kAttnRows][2]>(Qs);
+    if (fin) {
+      ml[hf][i][0] = m;
+      ml[hf][i][1] = l;
+    }
+    attn_bar_sync(1, 256);  // every softmax thread, whatever happened above
+    if (fin) {
       ptx::tc_fence_after_sync();
+      const float m0 = ml[0][i][0], l0 = ml[0][i][1], m1 = ml[1][i][0], l1 = ml[1][i][1];
+      const float M = fmaxf(m0, m1);
+      const float w0 = l0 > 0.f ? exp2f(m0 - M) : 0.f, w1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
+      const float L = w0 * l0 + w1 * l1;
       const int h = g * G + hq;
       float *dst;
       float inv = 1.f;
       if (a.splits == 1) {
         dst = a.o + (size_t(t0 + t) * a.Hq + h) * D;
-        inv = 1.f / l;
+        inv = 1.f / L;
       } else {
         const size_t wrow = ((((size_t(r) * a.Hkv + g) * a.tiles + tile) * a.splits + split) * kAttnRows) + i;
         dst = a.ws_o + wrow * D;
-        if (row_ok) {
-          a.ws_ml[2 * wrow] = m;
-          a.ws_ml[2 * wrow + 1] = l;
+        if (row_ok && hf == 0) {
+          a.ws_ml[2 * wrow] = M;
+          a.ws_ml[2 * wrow + 1] = L;
         }
       }
+      const int cb = hf * (D / 2);  // each half writes half of the output columns
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float x[16];
-        ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(c0), x);
+      for (int c0 = 0; c0 < D / 2; c0 += 16) {
+        float x0[16], x1[16];
+        ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(cb + c0), x0);
+        ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(D + cb + c0), x1);
         if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float a0 = w0 > 0.f ? w0 * x0[e] : 0.f, a1 = w1 > 0.f ? w1 * x1[e] : 0.f;
+            x0[e] = (a0 + a1) * inv;
+          }
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4 *>(dst + c0 + e) = make_float4(x[e] * inv, x[e + 1] * inv, x[e + 2] * inv,
-                                                                    x[e + 3] * inv);
+            *reinterpret_cast<float4 *>(dst + cb + c0 + e) = make_float4(x0[e], x0[e + 1], x0[e + 2], x0[e + 3]);
         }
       }
-    } else if (ok && nb == 0 && a.splits > 1 && row_ok) {  // an empty split: weight zero in the merge
+    } else if (ok && nb == 0 && a.splits > 1 && row_ok && hf == 0) {  // an empty split: weight zero
       const size_t wrow = ((((size_t(r) * a.Hkv + g) * a.tiles + tile) * a.splits + split) * kAttnRows) + i;
       a.ws_ml[2 * wrow] = -INFINITY;
       a.ws_ml[2 * wrow + 1] = 0.f;
