@@ -34,10 +34,11 @@ __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t b) {
   return make_float2(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
 }
 
-// Register cap per thread, sized so that 14 (four nodes), 11 (six) or 9 (eight) 64-thread CTAs
-// share an SM.
+// Register cap per thread, sized so that 14 (four nodes), 12 (six) or 9 (eight) 64-thread CTAs
+// share an SM (measured: 80 registers for six nodes beat 88 by 14 %; 72 for four nodes beat 68
+// and 64, which spill more).
 __host__ __device__ constexpr int stream_max_regs(int nmax, bool fuse) {
-  return fuse ? (nmax <= 4 ? 96 : nmax <= 6 ? 112 : 128) : (nmax <= 4 ? 72 : nmax <= 6 ? 88 : 112);
+  return fuse ? (nmax <= 4 ? 96 : nmax <= 6 ? 112 : 128) : (nmax <= 4 ? 72 : nmax <= 6 ? 80 : 112);
 }
 
 constexpr int kFuseMaxPath = 4;  // accepted-path entries the fused kernel folds in (u_j kept in registers)
