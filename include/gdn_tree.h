@@ -15,7 +15,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All array arguments are DEVICE pointers owned by the caller. The library allocates
- *    nothing, keeps no state between calls and never synchronises the device: each call
+ *    nothing, keeps no state between calls (gdn_tree_attention_noalloc's built-in scratch,
+ *    described there, is the one exception) and never synchronises the device: each call
  *    validates its scalar arguments on the host, enqueues its kernels on `stream` and
  *    returns. Results are valid once the stream has reached that point.
  *  - Layouts (T = node rows allocated, T >= cu_nodes[B]; all row-major, innermost last):
