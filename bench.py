@@ -256,6 +256,17 @@ def oracle_step(sb):
                   sb.path_len)
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(tb, target_s: float = 12.0) -> dict:
     """Time the oracle as it stands (OpenMP over pairs, all host cores) on a bounded sample of
     the workload: the first R requests with all heads, R sized for about target_s seconds."""
@@ -270,7 +281,7 @@ def cpu_baseline(tb, target_s: float = 12.0) -> dict:
     oracle_step(sb)
     dt = time.perf_counter() - t
     nodes = int(sb.cu_nodes[-1])
-    return {"value": nodes / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+    return {"value": nodes / dt, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(), "kind": "oracle",
             "sample": f"first {R} of {tb.B} requests x all {tb.H} heads (verify + commit replay, fp64), "
                       f"{dt:.1f} s"}
 
@@ -298,7 +309,8 @@ def run_reference(args):
             "steps": steps, "warmup": warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args.config, tb.B), "sample_per_step": f"{R} request(s) x {tb.H} heads"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "cpu_model": cpu_model(),
+                             "kind": "oracle",
                              "sample": f"{R} request(s) x all {tb.H} heads per step, verify + commit replay"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
