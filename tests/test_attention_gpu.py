@@ -98,3 +98,24 @@ def test_errors_are_reported_and_requests_skipped():
     assert np.all(np.isnan(o[ab.cu_nodes[1]:ab.cu_nodes[2]]))
     o, st = _run(ab, max_prefix=int(np.diff(ab.cu_prefix).min()) - 1)  # a prefix longer than max_prefix
     assert st & gb.STATUS_BAD_OFFSETS
+
+
+@pytest.mark.parametrize("Hq,Hkv,n_range", [(64, 2, (1, 16)), (128, 1, (1, 20))], ids=["g32", "g128"])
+def test_wide_query_groups(Hq, Hkv, n_range):
+    """Query-head groups of 32 and 128 (4 nodes, then 1 node, per 128-row tile: up to 20 tiles)."""
+    ab = W.make_attention_batch(40 + Hq, B=3, Hq=Hq, Hkv=Hkv, d=128, prefix_range=(64, 400), n_range=n_range)
+    for ws in (True, False):
+        o, st = _run(ab, workspace=ws)
+        assert st == 0
+        _check(ab, o, f"G={Hq // Hkv} {'split' if ws else 'nosplit'}")
+
+
+def test_bounds_larger_than_the_data():
+    """max_nodes / max_prefix above the actual sizes: the extra tiles and key splits find no rows
+    or no keys and must leave the result unchanged."""
+    ab = W.make_attention_batch(51, B=4, Hq=16, Hkv=2, d=128, prefix_range=(0, 500), n_range=(1, 9))
+    o_tight, st1 = _run(ab)
+    o_loose, st2 = _run(ab, max_nodes=64, max_prefix=6000)
+    assert st1 == 0 and st2 == 0
+    _check(ab, o_loose, "loose bounds")
+    assert float(np.max(np.abs(o_loose - o_tight))) <= 2.0 ** -8 * 5
