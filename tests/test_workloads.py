@@ -108,3 +108,51 @@ def test_state_distribution():
     tb = W.make_config(1, batch=8)
     s = tb.ST0.astype(np.float64)
     assert abs(s.std() - 0.1) < 0.005 and abs(s.mean()) < 0.005
+
+
+def test_serving_batch_recipe():
+    tb, sv = W.make_serving_batch(seed=4, B=9, H=8, H_qk=2, d=16, n_range=(1, 7), n_slots=30, pad_every=4)
+    assert sv.pool.shape == (30, 8, 16, 16) and sv.pool.dtype == np.float32
+    assert sv.q.shape == (tb.T, 2, 16) and sv.k.shape == (tb.T, 2, 16) and sv.q.dtype == np.uint16
+    live = sv.slot[sv.slot >= 0]
+    assert len(set(live.tolist())) == len(live) and np.all(live < 30)  # distinct slots inside the pool
+    assert sv.slot[3] == -1 and sv.slot[7] == -1 and np.sum(sv.slot == -1) == 2
+    assert abs(sv.q_scale - 16 ** -0.5) < 1e-12
+    assert np.all(sv.dt_bias >= -7) and np.all(sv.dt_bias <= -2)
+    assert np.all(np.exp(sv.A_log) >= 1 - 1e-6) and np.all(np.exp(sv.A_log) <= 16 + 1e-5)
+    # L2-normalised keys before bf16 rounding
+    k = W.bf16_bits_to_f32(sv.k)
+    np.testing.assert_allclose(np.linalg.norm(k, axis=-1), 1.0, atol=2e-2)
+    tb2, sv2 = W.make_serving_batch(seed=4, B=9, H=8, H_qk=2, d=16, n_range=(1, 7), n_slots=30, pad_every=4)
+    assert np.array_equal(sv.slot, sv2.slot) and np.array_equal(sv.a_raw, sv2.a_raw)
+    with pytest.raises(ValueError):
+        W.make_serving_batch(seed=4, B=9, H=8, H_qk=2, d=16, n_slots=5)
+
+
+def test_acceptance_draws_have_the_reported_spread():
+    rng = np.random.default_rng(0)
+    p = W.draw_acceptance(rng, 4096, 7)
+    assert p.dtype == np.float32 and np.all((p >= 0) & (p <= 1))
+    s = np.cumprod(p.astype(np.float64), axis=1)
+    assert s[:, 0].mean() > 0.7 and s[:, 6].mean() < 0.1  # first of seven drafts > 70 %, last < 10 %
+
+
+def test_candidate_tree_draws():
+    rng = np.random.default_rng(1)
+    fanout, depth = 3, 4
+    p = W.draw_edge_probs(rng, 5, fanout, depth)
+    C = sum(fanout ** l for l in range(depth + 1))
+    assert p.shape == (5, C) and np.all(p[:, 0] == 1)
+    kids = p[:, 1:].reshape(5, -1, fanout)
+    assert np.all(np.diff(kids, axis=2) <= 0)  # siblings sorted, most likely first
+    assert np.all(kids.sum(axis=2) <= 1 + 1e-6)  # one Dirichlet draw shared with "none accepted"
+
+
+def test_attention_batch_layout():
+    parents = [W.root_branch_parents(), W.chain_parents(3)]
+    ab = W.make_attention_batch(2, B=2, Hq=8, Hkv=2, d=64, prefix_range=(5, 9), parents=parents)
+    assert ab.T == 9 and ab.cu_nodes.tolist() == [0, 6, 9]
+    assert ab.q.shape == (9, 8, 64) and ab.k.shape == (9, 2, 64) and ab.v.shape == (9, 2, 64)
+    assert ab.k_cache.shape == (ab.P, 2, 64) and 10 <= ab.P <= 18
+    assert np.all(np.diff(ab.cu_prefix) >= 5) and np.all(np.diff(ab.cu_prefix) <= 9)
+    assert abs(ab.scale - 64 ** -0.5) < 1e-12 and ab.max_nodes == 6
