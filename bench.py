@@ -485,6 +485,50 @@ def run_ours(args):
                 "traffic": ncu_traffic(dom, wl), "nominal_peak": NOMINAL_HBM_GBS,
                 "frac_of_nominal": kernels[dom]["GB/s"] / NOMINAL_HBM_GBS}
 
+    # the store-all comparison the TreeWY page measures against: every node's state written
+    # (T x H x d_k x d_v fp32 of snapshots per layer), commit = copy of the accepted one
+    storeall = None
+    if args.storeall:
+        tb, d, o = layers[0], dev_in[0], dev_out[0]
+        snap = torch.empty((tb.T, tb.H, tb.dk, tb.dv), device=dev)
+        st_sa = torch.zeros(4, dtype=torch.int32, device=dev)
+
+        def sa_verify():
+            gb.gdn_tree_verify_storeall(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"],
+                                        d["cu_nodes"], tb.B, tb.H, tb.T, tb.dk, tb.dv, tb.max_nodes, snap, o["o"],
+                                        o["U"], o["G"], st_sa, stream)
+
+        def sa_commit():
+            gb.gdn_tree_commit_storeall(d["ST"], snap, d["parent"], d["cu_nodes"], d["path"], d["path_len"], tb.B,
+                                        tb.H, tb.T, tb.dk, tb.dv, tb.max_path, st_sa, stream)
+
+        for _ in range(3):
+            sa_verify()
+            sa_commit()
+        ns = 20
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        t_v = t_c = 0.0
+        for _ in range(ns):
+            evs[0].record(stream)
+            sa_verify()
+            evs[1].record(stream)
+            sa_commit()
+            evs[2].record(stream)
+            torch.cuda.synchronize()
+            t_v += evs[0].elapsed_time(evs[1])
+            t_c += evs[1].elapsed_time(evs[2])
+        if int(st_sa[0].item()):
+            raise RuntimeError("device reported data errors in the store-all comparison")
+        snap_bytes = snap.numel() * 4
+        storeall = {"verify_ms": t_v / ns, "commit_ms": t_c / ns, "step_ms": (t_v + t_c) / ns,
+                    "snapshot_bytes": snap_bytes,
+                    "treewy_speculative_bytes": tb.T * tb.H * (tb.dv + 1) * 4,
+                    "treewy_step_ms": v_ms + c_ms,
+                    "note": "gdn_tree_verify_storeall + gdn_tree_commit_storeall on one layer of the same "
+                            "workload; TreeWY keeps U and G (treewy_speculative_bytes) instead of every "
+                            "node's state (snapshot_bytes)"}
+        del snap
+
     # draft budgeting on the device: top-B positions (7 drafts per request, 3 per request on
     # average) and best-first growth over a ternary candidate tree of depth 7, at the batch size
     budget = None
@@ -644,7 +688,7 @@ def run_ours(args):
                 "frac": kernels["commit_verify"]["frac"], "steps": K, "gpu_launches": K,
                 "note": "gdn_tree_commit_verify: each step commits the previous step's accepted paths and verifies "
                         "the next trees in one pass over the state (deferred commit); same work as verify + commit"},
-            "graph_step": graph_step, "tree_budget": budget, "tree_attention": attention, "kernels": kernels,
+            "graph_step": graph_step, "storeall": storeall, "tree_budget": budget, "tree_attention": attention, "kernels": kernels,
             "wall_s_timed": wall}
     if rank == 0:
         print(json.dumps(line))
@@ -667,6 +711,8 @@ def main(argv=None):
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-storeall", dest="storeall", action="store_false",
+                    help="skip timing the store-all comparison (every node's state written)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from CUDA graphs (which removes the per-call host work)")
     ap.add_argument("--no-attention", dest="attention", action="store_false",
