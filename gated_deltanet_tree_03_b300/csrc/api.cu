@@ -1,12 +1,15 @@
 // Host side of the C ABI declared in include/gdn_tree.h: argument checks, launch
 // configuration, TMA descriptor encoding and kernel dispatch. Nothing here allocates device
-// memory, synchronises the device or keeps per-call state; the one fixed buffer is the scratch
-// array of gdn_tree_attention_noalloc (with its per-device address, looked up once).
+// memory, synchronises the device or keeps per-call state. What is kept across calls is
+// looked up once per device and never changes afterwards: the device's properties, each
+// kernel's dynamic shared-memory limit, and the address of the scratch array of
+// gdn_tree_attention_noalloc (its one fixed buffer).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <unordered_map>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -27,16 +30,90 @@ using namespace gdn;
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest shared memory one block may use on this architecture (227 KiB), for host-side size checks
+// that must not depend on a device being present.
+constexpr size_t kSmemPerBlockMax = 232448;
 bool valid_d(int d) { return d == 32 || d == 64 || d == 128; }
 
+// Properties of one device, queried on the first call that runs on it.
+struct DeviceInfo {
+  int major = 0, minor = 0;
+  int sms = 0;    // streaming multiprocessors
+  int optin = 0;  // opt-in dynamic + static shared memory per block, bytes
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev_info[kMaxDevices];
+bool g_dev_known[kMaxDevices] = {};
+
+// The current device's properties (one cudaGetDevice per call after the first on a device).
+gdn_status device_info(const DeviceInfo **out, int *dev_out = nullptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ECUDA;
+  if (dev_out) *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_dev_known[dev]) {
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return GDN_ECUDA;
+    g_dev_info[dev] = d;
+    g_dev_known[dev] = true;
+  }
+  *out = &g_dev_info[dev];
+  return GDN_OK;
+}
+
 gdn_status check_device() {
+  const DeviceInfo *d = nullptr;
+  const gdn_status st = device_info(&d);
+  if (st != GDN_OK) return st;
+  if (d->major != 10 || d->minor != 3) return GDN_EARCH;
+  return GDN_OK;
+}
+
+// Per (kernel, device): its static shared memory and the dynamic shared-memory limit set so
+// far. cudaFuncSetAttribute is called only when a launch needs more than the limit already set.
+struct FuncInfo {
+  int static_smem = -1;
+  int dyn_limit = 0;
+};
+std::mutex g_func_mu;
+std::unordered_map<uint64_t, FuncInfo> g_func_info;
+
+uint64_t func_key(const void *fn, int dev) { return (reinterpret_cast<uint64_t>(fn) << 6) ^ uint64_t(dev); }
+
+// Static shared memory of `fn` on the current device (looked up once).
+gdn_status func_static_smem(const void *fn, int *bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ECUDA;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+  std::lock_guard<std::mutex> lock(g_func_mu);
+  FuncInfo &fi = g_func_info[func_key(fn, dev)];
+  if (fi.static_smem < 0) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GDN_ECUDA;
+    fi.static_smem = int(fa.sharedSizeBytes);
+  }
+  *bytes = fi.static_smem;
+  return GDN_OK;
+}
+
+// Make sure `fn` may be launched with `bytes` of dynamic shared memory on the current device.
+gdn_status ensure_dyn_smem(const void *fn, size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ECUDA;
+  std::lock_guard<std::mutex> lock(g_func_mu);
+  FuncInfo &fi = g_func_info[func_key(fn, dev)];
+  if (size_t(fi.dyn_limit) >= bytes) return GDN_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess) {
+    (void)cudaGetLastError();  // the refused attribute must not surface as a later launch error
     return GDN_ECUDA;
-  if (major != 10 || minor != 3) return GDN_EARCH;
+  }
+  fi.dyn_limit = int(bytes);
   return GDN_OK;
 }
 
@@ -172,9 +249,7 @@ bool is_plain(const Serving &L) { return !L.slot && L.grp == 1 && L.q_scale == 1
 template <int DK, bool SV>
 gdn_status launch_verify_simt_sv(const VerifyArgs &a, const Serving &L, cudaStream_t stream) {
   const size_t smem = verify_simt_smem_bytes(a.max_nodes, DK);
-  if (cudaFuncSetAttribute(verify_simt_kernel<DK, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(smem)) != cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(reinterpret_cast<const void *>(verify_simt_kernel<DK, SV>), smem) != GDN_OK) return GDN_ECUDA;
   dim3 grid(a.dv / 32, a.H, a.B);
   verify_simt_kernel<DK, SV><<<grid, kThreads, smem, stream>>>(a, L);
   return launch_status();
@@ -186,10 +261,8 @@ gdn_status launch_verify_simt(const VerifyArgs &a, const Serving &L, cudaStream_
 }
 
 int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return n;
+  const DeviceInfo *d = nullptr;
+  return device_info(&d) == GDN_OK ? d->sms : 0;
 }
 
 template <int DK, int DV, bool SV>
@@ -201,14 +274,12 @@ gdn_status launch_verify_tc_sv(const VerifyArgs &a, const Serving &L, cudaStream
       !encode_rows(&tq, a.q, DK, HK, a.T, 64, Np, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_rows(&tv, a.v, DV, a.H, a.T, DV, Np, CU_TENSOR_MAP_SWIZZLE_NONE))
     return GDN_ECUDA;
-  int dev = 0, optin = 0;
-  cudaFuncAttributes fa{};
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaFuncGetAttributes(&fa, verify_tc_kernel<DK, DV, SV>) != cudaSuccess)
-    return GDN_ECUDA;
+  const DeviceInfo *di = nullptr;
+  int static_smem = 0;
+  const void *fn = reinterpret_cast<const void *>(verify_tc_kernel<DK, DV, SV>);
+  if (device_info(&di) != GDN_OK || func_static_smem(fn, &static_smem) != GDN_OK) return GDN_ECUDA;
   // deepest state ring that fits next to the node stages (1 KiB slack aligns the base)
-  const long long room = (long long)optin - (long long)fa.sharedSizeBytes - 1024;
+  const long long room = (long long)di->optin - (long long)static_smem - 1024;
   int R = kMaxRing;
   while (R > 2 && (long long)tc_layout(DK, DV, Np, R).total > room) --R;
   const TcLayout lay = tc_layout(DK, DV, Np, R);
@@ -216,11 +287,9 @@ gdn_status launch_verify_tc_sv(const VerifyArgs &a, const Serving &L, cudaStream
   // at least ~half an SM's shared memory, so a second CTA never waits on this one's tensor memory
   size_t smem = size_t(lay.total) + 1024;
   if (smem < 120u * 1024u) smem = 120u * 1024u;
-  if (cudaFuncSetAttribute(verify_tc_kernel<DK, DV, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(smem)) != cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(fn, smem) != GDN_OK) return GDN_ECUDA;
   const long long pairs = (long long)a.B * a.H;
-  const int sms = sm_count();
+  const int sms = di->sms;
   if (sms <= 0) return GDN_ECUDA;
   const unsigned grid = unsigned(pairs < sms ? pairs : sms);
   verify_tc_kernel<DK, DV, SV><<<grid, kTcThreads, smem, stream>>>(tk, tq, tv, a, lay, L);
@@ -264,9 +333,7 @@ gdn_status launch_verify_stream_dims(const VerifyArgs &a, const PrevCommit &c, c
 template <int DK, int DV, bool SV>
 gdn_status launch_commit_sv(const CommitArgs &a, const Serving &L, cudaStream_t stream) {
   const size_t smem = commit_smem_bytes(a.max_path, DK, DV);
-  if (cudaFuncSetAttribute(commit_kernel<DK, DV, SV>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-      cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(reinterpret_cast<const void *>(commit_kernel<DK, DV, SV>), smem) != GDN_OK) return GDN_ECUDA;
   const long long blocks = (long long)a.B * a.H;
   commit_kernel<DK, DV, SV><<<unsigned(blocks), kThreads, smem, stream>>>(a, L);
   return launch_status();
@@ -434,9 +501,7 @@ gdn_status launch_attention(const uint16_t *q, const uint16_t *k, const uint16_t
       !encode_rows(&tvt, v, D, a.Hkv, a.T, 64, kAttnTreeKeys, CU_TENSOR_MAP_SWIZZLE_128B))
     return GDN_ECUDA;
   const uint32_t smem = attn_smem_bytes(D);
-  if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-      cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(reinterpret_cast<const void *>(tree_attention_kernel<D>), smem) != GDN_OK) return GDN_ECUDA;
   dim3 grid(unsigned(a.tiles * a.splits), unsigned(a.Hkv), unsigned(a.B));
   tree_attention_kernel<D><<<grid, kAttnThreads, smem, s>>>(tq, tkc, tvc, tkt, tvt, a);
   gdn_status st = launch_status();
@@ -456,7 +521,6 @@ static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[kAttnNoAll
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[kMaxDevices] = {};
 
@@ -642,6 +706,9 @@ gdn_status gdn_tree_budget_topb(const float *p_accept, int32_t R, int32_t K, int
                                 gdn_stream_t stream) {
   if (R < 0 || K < 1 || K > kMaxNodes - 1 || budget < 0) return GDN_EINVAL;
   if ((long long)R * K > kTopbMaxItems) return GDN_ETOOBIG;
+  // keys, staged probabilities and per-request counts all sit in one CTA's shared memory
+  const size_t topb_smem = size_t(R) * K * 12 + size_t(R) * 4;
+  if (topb_smem > kSmemPerBlockMax) return GDN_ETOOBIG;
   if (R == 0) return GDN_OK;
   if (!p_accept || !n_sel || (parent && !cu_nodes)) return GDN_EINVAL;
   const void *ptrs[] = {p_accept, n_sel, survival, cu_nodes, parent, status};
@@ -649,11 +716,9 @@ gdn_status gdn_tree_budget_topb(const float *p_accept, int32_t R, int32_t K, int
     if (p && !aligned16(p)) return GDN_EALIGN;
   gdn_status st;
   if ((st = check_device()) != GDN_OK) return st;
-  const size_t smem = size_t(R) * K * 12 + size_t(R) * 4;  // keys, staged probabilities, per-request counts
-  if (cudaFuncSetAttribute(topb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(reinterpret_cast<const void *>(topb_kernel), topb_smem) != GDN_OK) return GDN_ECUDA;
   TopbArgs a{p_accept, R, K, budget, n_sel, survival, cu_nodes, parent, status};
-  topb_kernel<<<1, kTopbThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  topb_kernel<<<1, kTopbThreads, topb_smem, reinterpret_cast<cudaStream_t>(stream)>>>(a);
   return launch_status();
 }
 
@@ -677,8 +742,7 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
   gdn_status st;
   if ((st = check_device()) != GDN_OK) return st;
   const size_t smem = size_t(C) * 8 + size_t(C) * 4;  // candidate keys (then output positions), values
-  if (cudaFuncSetAttribute(grow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-    return GDN_ECUDA;
+  if (ensure_dyn_smem(reinterpret_cast<const void *>(grow_kernel), smem) != GDN_OK) return GDN_ECUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GrowArgs a{p_edge, R, fanout, depth, int(C), max_nodes, threshold, n_nodes, cand, parent_local, value, status};
   grow_kernel<<<unsigned(R), kGrowThreads, smem, s>>>(a);
@@ -698,21 +762,24 @@ gdn_status gdn_tree_attention_noalloc(const uint16_t *q, const uint16_t *k, cons
   gdn_status st = check_attn_shape(B, H_q, H_kv, d, max_nodes, max_prefix);
   if (st != GDN_OK) return st;
   if (B == 0 || T == 0 || max_nodes == 0) return GDN_OK;
-  // the same key splits gdn_tree_attention plans with an unlimited workspace; refuse what does not fit
-  const size_t need = attn_plan(B, H_q, H_kv, d, max_nodes, max_prefix, ~size_t(0)).ws_bytes;
-  if (need > kAttnNoAllocScratchBytes) {
+  if (T < 0 || P_total < 0 || !std::isfinite(scale) || !(scale > 0.f)) return GDN_EINVAL;
+  // The key splits gdn_tree_attention makes with a workspace of the scratch's size: the same
+  // plan as with an unlimited workspace whenever that plan fits, else fewer splits (one split
+  // needs no scratch at all), so every valid size runs.
+  const size_t need = attn_plan(B, H_q, H_kv, d, max_nodes, max_prefix, kAttnNoAllocScratchBytes).ws_bytes;
+  if (need > kAttnNoAllocScratchBytes) {  // the planner never asks for more; kept as a guard
     fprintf(stderr, "gdn_tree_attention_noalloc: these sizes need %zu bytes of scratch, more than the built-in %zu\n",
             need, kAttnNoAllocScratchBytes);
     return GDN_ETOOBIG;
   }
-  if (T < 0 || P_total < 0 || !std::isfinite(scale) || !(scale > 0.f)) return GDN_EINVAL;
   void *scratch = nullptr;
   if (need > 0) {
     if ((st = check_device()) != GDN_OK) return st;
     if ((st = noalloc_scratch(&scratch)) != GDN_OK) return st;
   }
   return gdn_tree_attention(q, k, v, k_cache, v_cache, cu_prefix, parent, cu_nodes, B, H_q, H_kv, T, P_total, d,
-                            max_nodes, max_prefix, scale, o, scratch, need, status, stream);
+                            max_nodes, max_prefix, scale, o, scratch, need > 0 ? kAttnNoAllocScratchBytes : 0,
+                            status, stream);
 }
 
 size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, int32_t d, int32_t max_nodes,

@@ -15,10 +15,15 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All array arguments are DEVICE pointers owned by the caller. The library allocates
- *    nothing, keeps no state between calls (gdn_tree_attention_noalloc's built-in scratch,
+ *    nothing, keeps no data between calls (gdn_tree_attention_noalloc's built-in scratch,
  *    described there, is the one exception) and never synchronises the device: each call
  *    validates its scalar arguments on the host, enqueues its kernels on `stream` and
  *    returns. Results are valid once the stream has reached that point.
+ *  - Host cost: the first call on a device queries the device's properties and each kernel's
+ *    shared-memory limit once; later calls reuse them (thread-safe), so an eager call costs a
+ *    few microseconds of host time. A process that calls cudaDeviceReset must not call the
+ *    library again afterwards (the kernels' shared-memory limits set on the old context are
+ *    gone).
  *  - Layouts (T = node rows allocated, T >= cu_nodes[B]; all row-major, innermost last):
  *        ST        [B][H][d_k][d_v]  fp32   committed state S^T (S is d_v x d_k)
  *        q, k      [T][H][d_k]       bf16   (passed as uint16_t bit patterns)
@@ -64,7 +69,7 @@ typedef struct CUstream_st *gdn_stream_t;
 typedef enum gdn_status {
     GDN_OK = 0,
     GDN_EINVAL = 1,      /* null pointer, negative size, unsupported d_k / d_v              */
-    GDN_ETOOBIG = 2,     /* max_nodes > 64 or max_path > 64                                  */
+    GDN_ETOOBIG = 2,     /* max_nodes > 64, max_path > 64, or a size over a stated maximum   */
     GDN_EALIGN = 3,      /* an array is not 16-byte aligned                                  */
     GDN_ECUDA = 6,       /* a CUDA runtime call failed (no device, launch failure, ...)      */
     GDN_EARCH = 7        /* the current device cannot run sm_103a code                       */
@@ -299,7 +304,8 @@ gdn_status gdn_tree_commit_verify_ex(float *ST, const float *U_prev, const float
  *                               request r; values outside [0, 1] or NaN count as 0 and set
  *                               GDN_STATUS_BAD_PROB
  *   R, K, budget           in   requests, draft positions per request (1..63), positions to
- *                               verify in total (>= 0); R * K <= 16384
+ *                               verify in total (>= 0); R * K <= 16384 and 12 R K + 4 R
+ *                               <= 232448 (one CTA's shared memory), else GDN_ETOOBIG
  *   n_sel     [R]    out        positions chosen for request r - always its first n_sel[r]
  *   survival  [R][K] out        optional: s[r][i] = p[r][0] * ... * p[r][i] (fp32, in that order)
  *   cu_nodes  [R+1]  out        optional: the verify batch, one chain per request of 1 + n_sel[r]
@@ -389,15 +395,23 @@ size_t gdn_tree_attention_workspace_size(int32_t B, int32_t H_q, int32_t H_kv, i
  * offer as workspace. The pages have no counterpart of this entry point; it only moves the
  * workspace of the key splits into scratch the library owns.
  *
- * Same arguments and results as gdn_tree_attention, without workspace and workspace_bytes. It
- * makes the key splits gdn_tree_attention would make with gdn_tree_attention_workspace_size()
- * bytes of workspace, in a 32 MiB scratch array built into the library: every GPU that loads
- * the library holds those 32 MiB until the process exits. Sizes that need more scratch return
- * GDN_ETOOBIG (with a message on stderr) before anything is launched. It calls no allocator.
- * The first call that needs scratch on a device looks up the array's device address for that
- * device (make that first call before any stream capture). Every call shares the one array and
- * writes the parts it reads, so nothing needs clearing between calls, but two calls that overlap
- * on the GPU (other streams, other host threads) race on it.
+ * Same arguments and results as gdn_tree_attention, without workspace and workspace_bytes. Its
+ * key splits live in a 32 MiB scratch array built into the library. It makes the splits that
+ * gdn_tree_attention makes with a 32 MiB workspace: the same plan (and bit-identical results) as
+ * with gdn_tree_attention_workspace_size() bytes whenever that is at most 32 MiB, otherwise
+ * fewer splits (at worst none, which needs no scratch), so every valid size runs. A plan larger
+ * than the scratch cannot occur; the entry point would return GDN_ETOOBIG with a message on
+ * stderr before launching anything. It calls no allocator.
+ *
+ * The array is device memory of the library's module: the driver reserves it on a device when
+ * the module is first loaded there (under CUDA's default lazy loading, at the library's first
+ * use on that device), and keeps it until the process exits. The first call that needs scratch
+ * on a device also looks up the array's device address there and keeps it. So make a first call
+ * on each device before reserving the rest of its memory for a pool, and before any stream
+ * capture; after cudaDeviceReset the kept address is stale and this entry point must not be
+ * used again in that process. Every call shares the one array and writes the parts it reads,
+ * so nothing needs clearing between calls, but two calls that overlap on the GPU (other
+ * streams, other host threads) race on it.
  */
 gdn_status gdn_tree_attention_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                       const uint16_t *k_cache, const uint16_t *v_cache,

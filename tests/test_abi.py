@@ -137,6 +137,7 @@ def test_commit_ex_layout_host_checks(lay, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(K=0), gb.GDN_EINVAL), (dict(K=64), gb.GDN_EINVAL), (dict(budget=-1), gb.GDN_EINVAL),
     (dict(R=2341, K=7), gb.GDN_ETOOBIG), (dict(p=None), gb.GDN_EINVAL), (dict(n_sel=FAKE + 4), gb.GDN_EALIGN),
+    (dict(R=16384, K=1), gb.GDN_ETOOBIG),  # 16384 items, but 256 KiB of shared memory for one CTA
     (dict(cu=None), gb.GDN_EINVAL),  # parent without cu_nodes
     (dict(R=0), gb.GDN_OK)])
 def test_budget_topb_host_checks(kw, code):

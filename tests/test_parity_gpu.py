@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU fp64 replay oracle.
 
-Covers all five synthetic workload presets at their full sizes (sampled (request, head) pairs
-for the oracle where the whole batch would take it too long), tiny and ragged random trees in
+Covers all five synthetic workload presets at their full sizes, compared with the oracle over the
+whole output tensors (o, U, G) and the whole committed state (the tolerances are stated as a max
+over a configuration's outputs and a Frobenius norm over its batch state), tiny and ragged random trees in
 random topological orders, empty requests, the deepest (chain of 64) and widest (star of 64)
 trees, forests, every verify kernel (gdn_tree_verify takes the register-resident streaming
 kernel when max_nodes <= 8 and the tensor-core kernel above that; gdn_tree_verify_simt is the
@@ -15,7 +16,7 @@ import torch
 from gated_deltanet_tree_03_b300 import binding as gb
 from gated_deltanet_tree_03_b300 import device as gd
 from gated_deltanet_tree_03_b300 import workloads as W
-from gpu_util import check_commit, check_verify, run_gpu, sample_pairs
+from gpu_util import check_commit, check_verify, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -32,48 +33,43 @@ def test_chain3_d32_full(kernel):
 
 
 @pytest.mark.parametrize("kernel,max_nodes", [("wy", None), ("wy", 16), ("simt", None)])
-def test_chain4_B256_full_size_sampled(kernel, max_nodes):
+def test_chain4_B256_full(kernel, max_nodes):
     """Depth-3 chain (4 nodes), B=256, H=32, d=128: the streaming kernel (max_nodes = 4) and the
     tensor-core kernel (16)."""
     tb = W.make_config(1)  # B=256, H=32, d=128, chain of 4
     res = run_gpu(tb, verify=kernel, max_nodes=max_nodes)
     assert res["status"] == 0
-    assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["U"]))
-    pairs = sample_pairs(tb, 96, seed=1)
-    check_verify(tb, res, pairs, tag=f"chain4_B256/{kernel}")
-    check_commit(tb, res, pairs, tag=f"chain4_B256/{kernel}")
+    check_verify(tb, res, tag=f"chain4_B256/{kernel}")
+    check_commit(tb, res, tag=f"chain4_B256/{kernel}")
 
 
 @pytest.mark.parametrize("batch", [1, 64])
 @pytest.mark.parametrize("kernel,max_nodes", [("wy", None), ("wy", 32), ("simt", None)])
-def test_rootbranch6(batch, kernel, max_nodes):
+def test_rootbranch6_full(batch, kernel, max_nodes):
     tb = W.make_config(2, batch=batch)
     res = run_gpu(tb, verify=kernel, max_nodes=max_nodes)
     assert res["status"] == 0
-    pairs = None if batch == 1 else sample_pairs(tb, 96, seed=2)
-    check_verify(tb, res, pairs, tag=f"rootbranch6/B{batch}/{kernel}")
-    check_commit(tb, res, pairs, tag=f"rootbranch6/B{batch}/{kernel}")
+    check_verify(tb, res, tag=f"rootbranch6/B{batch}/{kernel}")
+    check_commit(tb, res, tag=f"rootbranch6/B{batch}/{kernel}")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_ragged16to64_B128_full_size_sampled(kernel):
+def test_ragged16to64_B128_full(kernel):
     tb = W.make_config(3)
     res = run_gpu(tb, verify=kernel)
     assert res["status"] == 0
-    assert np.all(np.isfinite(res["o"]))
-    pairs = sample_pairs(tb, 64, seed=3)
-    check_verify(tb, res, pairs, tag=f"ragged16to64/{kernel}")
-    check_commit(tb, res, pairs, tag=f"ragged16to64/{kernel}")
+    check_verify(tb, res, tag=f"ragged16to64/{kernel}")
+    check_commit(tb, res, tag=f"ragged16to64/{kernel}")
 
 
-@pytest.mark.parametrize("batch", [1, 8, 512])
-def test_tree32(batch):
+@pytest.mark.parametrize("batch", [1, 8, 32, 128, 256, 512])
+def test_tree32_full(batch):
+    """The batch sweep of 32-node trees, every batch size, one of its 48 layers' input sets each."""
     tb = W.make_config(4, batch=batch, layer=batch % 48)
     res = run_gpu(tb, verify="wy")
     assert res["status"] == 0
-    pairs = sample_pairs(tb, 64, seed=4)
-    check_verify(tb, res, pairs, tag=f"tree32/B{batch}")
-    check_commit(tb, res, pairs, tag=f"tree32/B{batch}")
+    check_verify(tb, res, tag=f"tree32/B{batch}")
+    check_commit(tb, res, tag=f"tree32/B{batch}")
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
