@@ -321,6 +321,150 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+# every preset batch, as the line's "workloads" object: (config, batch, layers rotated)
+WORKLOAD_SET = [(0, 1, 4), (1, 256, 4), (2, 1, 4), (2, 64, 4), (3, 128, 4), (4, 1, 48), (4, 8, 48), (4, 32, 48),
+                (4, 128, 48), (4, 256, 48), (4, 512, 48)]
+L2_BYTES = 126 * 2 ** 20
+FLUSH_BYTES = 512 * 2 ** 20
+
+
+def layer_bytes(shape) -> int:
+    """HBM bytes one layer's verify + commit touch: state, node block, outputs."""
+    return shape.B * shape.H * shape.dk * shape.dv * 4 + shape.T * shape.H * (2 * shape.dk * 2 + shape.dv * 2 + 8 +
+                                                                              2 * shape.dv * 4 + 4)
+
+
+def time_workloads(gb, dev, stream, peaks, reps: int) -> dict:
+    """Every preset batch of the synthetic workloads, each over its own rotated layers (own state,
+    q, k, v, beta, g per layer; the batch sweep uses its 48 layers). Per pass (one layer's verify
+    then commit) the kernels are timed with CUDA events on the launching stream; when the rotated
+    working set is under 4x the L2, a 512 MB scratch write before each pass (outside the events)
+    evicts the previous passes' data. Values are drawn on the device with the presets' recipe."""
+    import torch
+    from gated_deltanet_tree_03_b300 import workloads as W
+    scratch = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for cfg, B, nl in WORKLOAD_SET:
+        shapes = [W.config_shape(cfg, B, l) for l in range(nl)]
+        layers = [W.draw_values_device(sh, seed=1000 * cfg + l, device=dev) for l, sh in enumerate(shapes)]
+        outs = [{"o": torch.empty(sh.T, sh.H, sh.dv, device=dev), "U": torch.empty(sh.T, sh.H, sh.dv, device=dev),
+                 "G": torch.empty(sh.T, sh.H, device=dev), "U2": torch.empty(sh.T, sh.H, sh.dv, device=dev),
+                 "G2": torch.empty(sh.T, sh.H, device=dev)} for sh in shapes]
+        status = torch.zeros(4, dtype=torch.int32, device=dev)
+        ws = sum(layer_bytes(sh) for sh in shapes)
+        flush = ws < 4 * L2_BYTES
+
+        def verify(j, U="U", G="G"):
+            sh, d, o = shapes[j], layers[j], outs[j]
+            gb.gdn_tree_verify(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"], d["cu_nodes"], sh.B,
+                               sh.H, sh.T, sh.dk, sh.dv, sh.max_nodes, o["o"], o[U], o[G], status, stream)
+
+        def commit(j, U="U", G="G"):
+            sh, d, o = shapes[j], layers[j], outs[j]
+            gb.gdn_tree_commit(d["ST"], o[U], o[G], d["k"], d["parent"], d["cu_nodes"], d["path"], d["path_len"],
+                               sh.B, sh.H, sh.T, sh.dk, sh.dv, sh.max_path, status, stream)
+
+        for j in range(min(nl, 3)):
+            verify(j)
+            commit(j)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for r in range(reps):
+            if flush:
+                scratch.fill_(float(r))
+            j = r % nl
+            ev[r][0].record(stream)
+            verify(j)
+            ev[r][1].record(stream)
+            commit(j)
+            ev[r][2].record(stream)
+        torch.cuda.synchronize()
+        v_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / reps
+        c_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / reps
+        # commit folded into the next verify (gdn_tree_commit_verify); pseudo-values alternate between
+        # two buffers per layer so that each call commits the previous call's accepted paths
+        cur = [0] * nl
+        for j in range(nl):
+            verify(j)
+
+        def fused(j):
+            sh, d, o = shapes[j], layers[j], outs[j]
+            (Up, Gp), (Un, Gn) = ((o["U"], o["G"]), (o["U2"], o["G2"]))[::1 if cur[j] == 0 else -1]
+            gb.gdn_tree_commit_verify(d["ST"], Up, Gp, d["k"], d["parent"], d["cu_nodes"], d["path"], d["path_len"],
+                                      sh.T, sh.max_path, d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"],
+                                      d["cu_nodes"], sh.B, sh.H, sh.T, sh.dk, sh.dv, sh.max_nodes, o["o"], Un, Gn,
+                                      status, stream)
+            cur[j] = 1 - cur[j]
+
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for r in range(reps):
+            if flush:
+                scratch.fill_(float(r))
+            fev[r][0].record(stream)
+            fused(r % nl)
+            fev[r][1].record(stream)
+        torch.cuda.synchronize()
+        f_ms = sum(e[0].elapsed_time(e[1]) for e in fev) / reps
+        # back-to-back steps (no flush) from Python and replayed from CUDA graphs: how much of a
+        # small batch's step is host time
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for r in range(reps):
+            verify(r % nl)
+            commit(r % nl)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = e0.elapsed_time(e1) / reps
+        graph_ms = None
+        if B <= 8:
+            graphs = []
+            for j in range(nl):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    cs = torch.cuda.current_stream()
+                    sh, d, o = shapes[j], layers[j], outs[j]
+                    gb.gdn_tree_verify(d["ST"], d["q"], d["k"], d["v"], d["beta"], d["g"], d["parent"],
+                                       d["cu_nodes"], sh.B, sh.H, sh.T, sh.dk, sh.dv, sh.max_nodes, o["o"], o["U"],
+                                       o["G"], status, cs)
+                    gb.gdn_tree_commit(d["ST"], o["U"], o["G"], d["k"], d["parent"], d["cu_nodes"], d["path"],
+                                       d["path_len"], sh.B, sh.H, sh.T, sh.dk, sh.dv, sh.max_path, status, cs)
+                graphs.append(gr)
+            for j in range(nl):
+                graphs[j].replay()
+            torch.cuda.synchronize()
+            e0.record()
+            for r in range(reps):
+                graphs[r % nl].replay()
+            e1.record()
+            torch.cuda.synchronize()
+            graph_ms = e0.elapsed_time(e1) / reps
+            del graphs
+        if int(status[0].item()):
+            raise RuntimeError(f"device reported data errors (status {int(status[0].item()):#x}) in workload {cfg}/{B}")
+
+        vb = float(np.mean([verify_bytes(sh) for sh in shapes]))
+        cb = float(np.mean([commit_bytes(sh) for sh in shapes]))
+        fb = float(np.mean([fused_bytes(sh) for sh in shapes]))
+        T = float(np.mean([sh.T for sh in shapes]))
+        pk = peaks["hbm_gbs"]
+        gbs = lambda b, ms: b / (ms * 1e6)
+        key = f"{WORKLOAD_NAMES[cfg][0]}_B{B}"
+        out[key] = {
+            "workload": workload_name(cfg, B), "layers_rotated": nl, "node_rows": T, "reps": reps,
+            "l2": (f"flushed: {FLUSH_BYTES >> 20} MB scratch write before each pass (working set {ws / 2 ** 20:.0f} MB "
+                   f"< 4x L2)") if flush else f"rotated: working set {ws / 2 ** 20:.0f} MB >= 4x L2",
+            "verify_ms": v_ms, "commit_ms": c_ms, "step_ms": v_ms + c_ms, "fused_ms": f_ms,
+            "eager_step_ms_back_to_back": eager_ms, "graph_step_ms": graph_ms,
+            "verify_frac": gbs(vb, v_ms) / pk, "commit_frac": gbs(cb, c_ms) / pk,
+            "step_frac": gbs(vb + cb, v_ms + c_ms) / pk, "fused_frac": gbs(fb, f_ms) / pk,
+            "step_frac_of_nominal": gbs(vb + cb, v_ms + c_ms) / NOMINAL_HBM_GBS,
+            "node_verifications_per_s": T / ((v_ms + c_ms) / 1e3),
+            "node_verifications_per_s_fused": T / (f_ms / 1e3),
+        }
+        del layers, outs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -378,9 +522,19 @@ def run_ours(args):
     clk = clocks.stop()
     if dist is not None:
         dist.barrier()
-    t_ver = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
-    t_com = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    # the per-kernel breakdown takes its own repeat count (independent of --steps)
+    Kr = max(1, args.kernel_reps)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kr)]
+    for i in range(Kr):
+        kev[i][0].record(stream)
+        tb, d, o = step(i)
+        kev[i][1].record(stream)
+        commit(tb, d, o)
+        kev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_ver = sum(kev[i][0].elapsed_time(kev[i][1]) for i in range(Kr))
+    t_com = sum(kev[i][1].elapsed_time(kev[i][2]) for i in range(Kr))
     total_ms = max_over_ranks(dist, total_ms, dev)
     nodes_per_step = tb0.T  # draft nodes of one layer's batch, all heads
     value = nodes_per_step * world * K / (total_ms / 1e3)
@@ -428,8 +582,9 @@ def run_ours(args):
     peaks = measured_peaks()
     vb = float(np.mean([verify_bytes(tb) for tb in layers]))
     cb = float(np.mean([commit_bytes(tb) for tb in layers]))
-    v_ms, c_ms = t_ver / K, t_com / K
+    v_ms, c_ms = t_ver / Kr, t_com / Kr
     kernels = {
+        "reps": Kr,
         "verify": {"ms": v_ms, "alg_bytes": vb, "GB/s": vb / (v_ms * 1e6), "frac": vb / (v_ms * 1e6) / peaks["hbm_gbs"]},
         "commit": {"ms": c_ms, "alg_bytes": cb, "GB/s": cb / (c_ms * 1e6), "frac": cb / (c_ms * 1e6) / peaks["hbm_gbs"]},
         "verify+commit": {"ms": v_ms + c_ms, "GB/s": (vb + cb) / ((v_ms + c_ms) * 1e6),
@@ -477,7 +632,8 @@ def run_ours(args):
                                     "frac": fb / (f_ms * 1e6) / peaks["hbm_gbs"],
                                     "node_verifications_per_s": nodes_per_step * world / (f_ms / 1e3)}
     for kd in kernels.values():
-        kd["frac_of_nominal"] = kd["GB/s"] / NOMINAL_HBM_GBS
+        if isinstance(kd, dict):
+            kd["frac_of_nominal"] = kd["GB/s"] / NOMINAL_HBM_GBS
     dom = "verify" if v_ms >= c_ms else "commit"
     wl = workload_key(args.config, tb0.B)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["GB/s"], "peak": peaks["hbm_gbs"],
@@ -673,13 +829,19 @@ def run_ours(args):
                "note": "state resident in HBM across steps; every step copies its node block, tree and paths in "
                        "from pinned host memory and its o out, on copy streams overlapping the neighbouring steps"}
 
+    workloads = None
+    if args.workloads and world == 1:
+        workloads = time_workloads(gb, dev, stream, peaks, args.kernel_reps)
+    ws = sum(layer_bytes(tb) for tb in layers)
+    l2 = (f"inputs larger than L2: {len(layers)} layers rotated, working set {ws / 2 ** 20:.0f} MB >= 4x L2"
+          if ws >= 4 * L2_BYTES else f"working set {ws / 2 ** 20:.0f} MB below 4x L2 (L2-warm; not flushed)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {"workload": workload_name(args.config, tb0.B), "batch_per_gpu": tb0.B, "heads": tb0.H,
                        "d_k": tb0.dk, "d_v": tb0.dv, "nodes_per_layer": nodes_per_step,
                        "layers_rotated": len(layers), "verify_kernel": args.kernel,
-                       "l2": "inputs larger than L2 (per-layer state > 126 MB; layers rotated)",
+                       "l2": l2,
                        "parallelism": f"dp{world} (independent batches per GPU)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * K, "clocks": clk,
             "fused_commit_verify": None if "commit_verify" not in kernels else {
@@ -688,7 +850,7 @@ def run_ours(args):
                 "frac": kernels["commit_verify"]["frac"], "steps": K, "gpu_launches": K,
                 "note": "gdn_tree_commit_verify: each step commits the previous step's accepted paths and verifies "
                         "the next trees in one pass over the state (deferred commit); same work as verify + commit"},
-            "graph_step": graph_step, "storeall": storeall, "tree_budget": budget, "tree_attention": attention, "kernels": kernels,
+            "workloads": workloads, "graph_step": graph_step, "storeall": storeall, "tree_budget": budget, "tree_attention": attention, "kernels": kernels,
             "wall_s_timed": wall}
     if rank == 0:
         print(json.dumps(line))
@@ -719,6 +881,10 @@ def main(argv=None):
                     help="skip timing tree-bias attention (gdn_tree_attention)")
     ap.add_argument("--no-budget", dest="budget", action="store_false",
                     help="skip timing the draft-budgeting kernels (top-B positions, best-first growth)")
+    ap.add_argument("--kernel-reps", type=int, default=200,
+                    help="passes behind the per-kernel breakdown and each workloads entry")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip timing every preset batch (the workloads object)")
     ap.add_argument("--no-fused", dest="fused", action="store_false",
                     help="skip timing gdn_tree_commit_verify (the previous step's commit folded into the next verify)")
     args = ap.parse_args(argv)

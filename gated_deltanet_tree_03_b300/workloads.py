@@ -526,3 +526,109 @@ def make_attention_batch(seed: int, B: int, Hq: int, Hkv: int, d: int, prefix_ra
     return AttentionBatch(B=B, Hq=Hq, Hkv=Hkv, d=d, parent=parent, cu_nodes=cu, cu_prefix=cp,
                           q=bf(T, Hq, d), k=bf(T, Hkv, d), v=bf(T, Hkv, d), k_cache=bf(P, Hkv, d),
                           v_cache=bf(P, Hkv, d), scale=float(d ** -0.5))
+
+
+# ---------------------------------------------------------------------------
+# the same presets drawn on a CUDA device (for timing many large layers)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class TreeShape:
+    """The integer part of one preset layer: trees and accepted paths, no values."""
+
+    B: int
+    H: int
+    dk: int
+    dv: int
+    parent: np.ndarray
+    cu_nodes: np.ndarray
+    path: np.ndarray
+    path_len: np.ndarray
+    gate: str
+    name: str = ""
+
+    @property
+    def T(self) -> int:
+        return int(self.cu_nodes[-1])
+
+    @property
+    def max_nodes(self) -> int:
+        return int(np.max(np.diff(self.cu_nodes))) if self.B else 0
+
+    @property
+    def max_path(self) -> int:
+        return int(self.path.shape[1])
+
+
+def config_shape(idx: int, batch: int | None = None, layer: int = 0) -> TreeShape:
+    """The trees and accepted paths of ``make_config(idx, batch, layer)`` (the same draws from
+    the same seed), without drawing the layer's values."""
+    if batch is None:
+        batch = CONFIG_BATCHES[idx][-1]
+    rng = np.random.default_rng(np.random.SeedSequence([idx, batch, layer]))
+    H, d, gate = 32, 128, "softplus"
+    parents, paths = [], []
+    if idx == 0:
+        parents, paths, H, d = [chain_parents(3)], [[0, 1]], 1, 32
+    elif idx == 1:
+        for _ in range(batch):
+            parents.append(chain_parents(4))
+            paths.append(list(range(int(rng.integers(0, 4)) + 1)))
+    elif idx == 2:
+        H = 48
+        for _ in range(batch):
+            p = root_branch_parents()
+            parents.append(p)
+            paths.append(greedy_walk_path(rng, p))
+    elif idx == 3:
+        for _ in range(batch):
+            p = random_tree_parents(rng, int(rng.integers(16, 65)), fanout_max=4, depth_max=8)
+            parents.append(p)
+            paths.append(leaf_prefix_path(rng, p))
+    elif idx == 4:
+        gate = "uniform"
+        for _ in range(batch):
+            p = random_tree_parents(rng, 32, fanout_max=3, depth_max=6)
+            parents.append(p)
+            paths.append(leaf_prefix_path(rng, p))
+    else:
+        raise ValueError(f"unknown config {idx}")
+    B = len(parents)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    cu[1:] = np.cumsum([len(p) for p in parents])
+    max_path = max([len(p) for p in paths] + [1])
+    path = np.full((B, max_path), -1, dtype=np.int32)
+    path_len = np.zeros(B, dtype=np.int32)
+    for r, p in enumerate(paths):
+        path[r, :len(p)] = p
+        path_len[r] = len(p)
+    parent = np.concatenate([np.asarray(p, dtype=np.int32) for p in parents])
+    return TreeShape(B=B, H=H, dk=d, dv=d, parent=parent, cu_nodes=cu, path=path, path_len=path_len, gate=gate,
+                     name=f"config{idx}_B{batch}_layer{layer}")
+
+
+def draw_values_device(shape: TreeShape, seed: int, device) -> dict:
+    """One layer's values for ``shape`` drawn on ``device`` with the presets' value recipe
+    (torch's seeded generator instead of numpy's): S ~ N(0, 0.1^2) fp32; q, k ~ N(0, 1)
+    L2-normalised in fp32 then rounded to bf16; v ~ N(0, 1) in bf16; beta ~ U(0, 1);
+    g = ln a with a = exp(-0.1 softplus(x)), x ~ N(0, 1), or a ~ U(0.85, 1)."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    T, H, dk, dv = shape.T, shape.H, shape.dk, shape.dv
+    f32 = dict(dtype=torch.float32, device=device, generator=gen)
+
+    def unit_rows(*s):
+        x = torch.randn(*s, **f32)
+        return (x / x.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+
+    out = {"ST": torch.randn(shape.B, H, dk, dv, **f32) * 0.1, "q": unit_rows(T, H, dk), "k": unit_rows(T, H, dk),
+           "v": torch.randn(T, H, dv, **f32).to(torch.bfloat16), "beta": torch.rand(T, H, **f32)}
+    if shape.gate == "uniform":
+        out["g"] = torch.log(0.85 + 0.15 * torch.rand(T, H, **f32))
+    else:
+        out["g"] = -0.1 * torch.nn.functional.softplus(torch.randn(T, H, **f32))
+    for key, arr in (("parent", shape.parent), ("cu_nodes", shape.cu_nodes), ("path", shape.path),
+                     ("path_len", shape.path_len)):
+        out[key] = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.int32)).to(device)
+    return out

@@ -156,3 +156,40 @@ def test_attention_batch_layout():
     assert ab.k_cache.shape == (ab.P, 2, 64) and 10 <= ab.P <= 18
     assert np.all(np.diff(ab.cu_prefix) >= 5) and np.all(np.diff(ab.cu_prefix) <= 9)
     assert abs(ab.scale - 64 ** -0.5) < 1e-12 and ab.max_nodes == 6
+
+
+@pytest.mark.parametrize("cfg,batch,layer", [(0, 1, 0), (1, 256, 0), (2, 1, 0), (2, 64, 0), (3, 128, 0), (4, 8, 7),
+                                             (4, 128, 47)])
+def test_config_shape_matches_make_config(cfg, batch, layer):
+    """The device-timed presets use the same trees and accepted paths as the host presets."""
+    s = W.config_shape(cfg, batch, layer)
+    t = W.make_config(cfg, batch=batch, layer=layer)
+    for key in ("parent", "cu_nodes", "path", "path_len"):
+        np.testing.assert_array_equal(getattr(s, key), getattr(t, key))
+    assert (s.B, s.H, s.dk, s.dv, s.T, s.max_nodes, s.max_path) == (t.B, t.H, t.dk, t.dv, t.T, t.max_nodes,
+                                                                     t.max_path)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_draw_values_device_recipe(cfg):
+    """Device-drawn values follow the preset recipe (drawn here on the CPU device)."""
+    import torch
+    s = W.config_shape(cfg, 64 if cfg == 2 else 32, 0)
+    v = W.draw_values_device(s, seed=5, device="cpu")
+    T, H = s.T, s.H
+    assert v["ST"].shape == (s.B, H, 128, 128) and v["ST"].dtype == torch.float32
+    assert abs(float(v["ST"].std()) - 0.1) < 0.005
+    for key in ("q", "k"):
+        assert v[key].shape == (T, H, 128) and v[key].dtype == torch.bfloat16
+        norms = v[key].float().norm(dim=-1)
+        assert float((norms - 1).abs().max()) < 0.02
+    assert v["v"].dtype == torch.bfloat16 and abs(float(v["v"].float().std()) - 1) < 0.05
+    assert float(v["beta"].min()) >= 0 and float(v["beta"].max()) <= 1
+    a = torch.exp(v["g"])
+    if cfg == 4:
+        assert float(a.min()) >= 0.85 - 1e-6 and float(a.max()) <= 1.0
+    else:
+        assert float(v["g"].max()) <= 0 and abs(float(v["g"].mean()) + 0.1 * 0.8) < 0.02  # E softplus(N(0,1)) ~ 0.806
+    again = W.draw_values_device(s, seed=5, device="cpu")
+    assert torch.equal(again["q"], v["q"])
+    np.testing.assert_array_equal(v["parent"].numpy(), s.parent)
