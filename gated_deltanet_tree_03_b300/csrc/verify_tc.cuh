@@ -119,11 +119,8 @@ struct __align__(16) TreeStage {
   float beta[kMaxNodes];
   float a[kMaxNodes];                 // exp(g): the node's gate
   int par[kMaxNodes];
-  int off[kMaxNodes + 1];             // packed per-path offsets: row t at off[t], depth(t)+1 entries
   uint8_t dep[kMaxNodes];
   uint8_t pj[kMaxNodes][12];          // paths of up to kRegPath nodes: p_0 .. p_d, then t repeated
-  int nent;                           // path entries of the pair
-  int maxd;
   int bad;
 };
 
@@ -186,12 +183,20 @@ __device__ __forceinline__ uint32_t sw128_bf16(int r, int j) {
   return uint32_t(r * 128 + ((((j * 2) >> 4) ^ (r & 7)) << 4) + ((j * 2) & 15));
 }
 
+// Round to bf16 (nearest even) by the hardware conversion.
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float x) {
+  uint16_t b;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(x));
+  return b;
+}
+
 // Store z as bf16 hi + lo at (row r, column j) of the [T ; W] operand.
 __device__ __forceinline__ void put_hilo(uint8_t *bop, uint32_t lo_off, int r, int j, float z) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(z), l = __float2bfloat16_rn(z - __bfloat162float(h));
+  const uint16_t h = f32_to_bf16_rn(z);
+  const uint16_t l = f32_to_bf16_rn(z - __uint_as_float(uint32_t(h) << 16));
   const uint32_t o = sw128_bf16(r, j);
-  *reinterpret_cast<__nv_bfloat16 *>(bop + o) = h;
-  *reinterpret_cast<__nv_bfloat16 *>(bop + lo_off + o) = l;
+  *reinterpret_cast<uint16_t *>(bop + o) = h;
+  *reinterpret_cast<uint16_t *>(bop + lo_off + o) = l;
 }
 
 template <int DK, int DV, bool SV>
@@ -330,8 +335,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::tc_fence_after_sync();
         const uint32_t x0 = ptx::smem_u32(base + lay.x);
         const uint32_t d1 = tmem + uint32_t(b) * bufcols, d2 = d1 + gcol;
-        // Gram: A = all 128 rows of X, B = the key rows
-#pragma unroll
+        // Gram: A = all 128 rows of X, B = the key rows (loops kept rolled: the kernel's roles
+        // together run more code than the instruction caches hold)
+#pragma unroll 1
         for (int ks = 0; ks < DK / 16; ++ks) {
           const uint64_t dx = ptx::desc_kmajor_sw128(x0 + (ks >> 2) * kRegionBytes + (ks & 3) * 32);
           ptx::mma_bf16_ss(d2, dx, dx, id_gram, ks > 0 ? 1u : 0u);
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (!tc_wait(&sh.slot_split[s], (u / R) & 1u, sh, a.status)) { ok = false; break; }
           ptx::tc_fence_after_sync();
           const uint32_t a_hi = ptx::smem_u32(ring + s * kSlotBytes), a_lo = a_hi + kRegionBytes;
-#pragma unroll
+#pragma unroll 1
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bx = ptx::desc_kmajor_sw128(x0 + c * kRegionBytes + kk * 32);
             ptx::mma_bf16_ss(d1, ptx::desc_kmajor_sw128(a_hi + kk * 32), bx, id_proj, (c | kk) ? 1u : 0u);
@@ -377,15 +383,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t ph = (i >> lgns) & 1u;
       // the pair's parents, gates and betas are read from global memory before the wait for a
       // free stage, so their latency overlaps it
-      int pr[2] = {0, 0};
-      float gg[2] = {0.f, 0.f}, bb[2] = {0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = lane + 32 * e;
-        if (t < n) {
-          pr[e] = a.parent[t0 + t];
-          gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + t) * a.H + h, h, gg[e], bb[e]);
-        }
+      // lane handles nodes lane and lane + 32
+      const int tA = lane, tB = lane + 32;
+      int prA = 0, prB = 0;
+      float gA = 0.f, gB = 0.f, bA = 0.f, bB = 0.f;
+      if (tA < n) {
+        prA = a.parent[t0 + tA];
+        gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tA) * a.H + h, h, gA, bA);
+      }
+      if (tB < n) {
+        prB = a.parent[t0 + tB];
+        gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tB) * a.H + h, h, gB, bB);
       }
       int ok = 1;
       if (lane == 0) ok = tc_wait(&sh.tree_empty[b], ph ^ 1u, sh, a.status);
@@ -393,27 +401,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::mbar_try_wait(&sh.tree_empty[b], ph ^ 1u);  // acquire for every lane
       TreeStage &ts = sh.tree[b];
       int bad = 0;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = lane + 32 * e;
-        if (t < n) {
-          bad |= (pr[e] < -1 || pr[e] >= t);
-          ts.par[t] = pr[e];
-          ts.beta[t] = bb[e];
-          ts.a[t] = gg[e];  // g for now; the gate exp(g) once every path sum is formed
-        }
+      if (tA < n) {
+        bad |= (prA < -1 || prA >= tA);
+        ts.par[tA] = prA;
+        ts.beta[tA] = bA;
+        ts.a[tA] = gA;  // g for now; the gate exp(g) once every path sum is formed
+      }
+      if (tB < n) {
+        bad |= (prB < -1 || prB >= tB);
+        ts.par[tB] = prB;
+        ts.beta[tB] = bB;
+        ts.a[tB] = gB;
       }
       bad = __any_sync(0xffffffffu, bad);
       __syncwarp();
-      int cnt[2] = {0, 0};
       if (!bad) {
-#pragma unroll
+        // ancestor masks and cumulative log-gates (parent indices strictly decrease along the
+        // walk, so it ends within t + 1 steps), then depths, gates and the node lists of paths
+        // short enough to be solved in registers
+#pragma unroll 1
         for (int e = 0; e < 2; ++e) {
-          const int t = lane + 32 * e;
+          const int t = e ? tB : tA;
           if (t < n) {
-            // parent indices strictly decrease along the walk, so it ends within t + 1 steps
             unsigned long long m = 1ull << t;
-            float Gs = gg[e];
+            float Gs = e ? gB : gA;
             for (int x = ts.par[t]; x >= 0; x = ts.par[x]) {
               m |= 1ull << x;
               Gs += ts.a[x];
@@ -421,35 +432,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ts.anc[t] = m;
             ts.G[t] = Gs;
             ts.gam[t] = expf(Gs);
-            cnt[e] = __popcll(m);
+            ts.dep[t] = uint8_t(__popcll(m) - 1);
           }
         }
-        // exclusive prefix sum of the ancestor counts over t = 0..n-1
-        int run = 0, offs[2] = {0, 0};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          int x = cnt[e];
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-          }
-          const int t = lane + 32 * e;
-          offs[e] = run + x - cnt[e];
-          if (t < n) ts.off[t] = offs[e];
-          run += __shfl_sync(0xffffffffu, x, 31);
-        }
-        // depths, gates, and the node lists of paths short enough to be solved in registers
         __syncwarp();
-        int dmax = 0;
-#pragma unroll
+#pragma unroll 1
         for (int e = 0; e < 2; ++e) {
-          const int t = lane + 32 * e;
+          const int t = e ? tB : tA;
           if (t < n) {
-            const int d = cnt[e] - 1;
-            ts.dep[t] = uint8_t(d);
-            dmax = max(dmax, d);
-            ts.a[t] = expf(gg[e]);
+            const int d = ts.dep[t];
+            ts.a[t] = expf(e ? gB : gA);
             if (d < kRegPath) {
               int x = t;
               for (int k = d; k >= 0; --k) {
@@ -459,11 +451,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               for (int k = d + 1; k < kRegPath; ++k) ts.pj[t][k] = uint8_t(t);
             }
           }
-        }
-        dmax = __reduce_max_sync(0xffffffffu, dmax);
-        if (lane == 0) {
-          ts.maxd = dmax;
-          ts.nent = run;
         }
       } else if (lane == 0 && h == 0) {
         report(a.status, GDN_STATUS_BAD_TREE);
