@@ -17,7 +17,7 @@ from . import _build
 
 GDN_OK, GDN_EINVAL, GDN_ETOOBIG, GDN_EALIGN, GDN_ECUDA, GDN_EARCH = 0, 1, 2, 3, 6, 7
 STATUS_BAD_TREE, STATUS_BAD_PATH, STATUS_TOO_MANY_NODES, STATUS_TIMEOUT, STATUS_BAD_OFFSETS = 1, 2, 4, 8, 16
-STATUS_PATH_TRUNCATED, STATUS_BAD_SLOT, STATUS_BAD_PROB = 32, 64, 128
+STATUS_PATH_TRUNCATED, STATUS_BAD_SLOT, STATUS_BAD_PROB, STATUS_OUT_OF_BOUNDS = 32, 64, 128, 256
 MAX_NODES = 64
 
 HEADER = os.path.join(_build.INCLUDE, "gdn_tree.h")
@@ -30,7 +30,8 @@ class GdnError(RuntimeError):
 
 
 def _load() -> ctypes.CDLL:
-    path = _build.build()
+    # GDN_TREE_DEBUG_BOUNDS=1 selects the address-checking build of the same kernels
+    path = _build.build(debug_bounds=os.environ.get("GDN_TREE_DEBUG_BOUNDS") == "1")
     return ctypes.CDLL(path)
 
 

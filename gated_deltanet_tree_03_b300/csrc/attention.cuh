@@ -31,6 +31,7 @@
 
 #include <cuda.h>
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -436,13 +437,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int h = g * G + hq;
       float *dst;
       float inv = 1.f;
+      bool dst_ok;  // (the debug build checks the row against its array)
       if (a.splits == 1) {
         dst = a.o + (size_t(t0 + t) * a.Hq + h) * D;
         inv = 1.f / L;
+        dst_ok = !row_ok || in_bounds((long long)(t0 + t) * a.Hq + h, (long long)a.T * a.Hq, a.status);
       } else {
         const size_t wrow = ((((size_t(r) * a.Hkv + g) * a.tiles + tile) * a.splits + split) * kAttnRows) + i;
         dst = a.ws_o + wrow * D;
-        if (row_ok && hf == 0) {
+        dst_ok = !row_ok || in_bounds((long long)wrow, (long long)a.B * a.Hkv * a.tiles * a.splits * kAttnRows, a.status);
+        if (row_ok && dst_ok && hf == 0) {
           a.ws_ml[2 * wrow] = M;
           a.ws_ml[2 * wrow + 1] = L;
         }
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         float x0[16], x1[16];
         ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(cb + c0), x0);
         ptx::tmem_ld_32x32b_x16(tmem + lane_addr + O_col + uint32_t(D + cb + c0), x1);
-        if (row_ok) {
+        if (row_ok && dst_ok) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float a0 = w0 > 0.f ? w0 * x0[e] : 0.f, a1 = w1 > 0.f ? w1 * x1[e] : 0.f;
@@ -466,8 +470,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     } else if (ok && nb == 0 && a.splits > 1 && row_ok && hf == 0) {  // an empty split: weight zero
       const size_t wrow = ((((size_t(r) * a.Hkv + g) * a.tiles + tile) * a.splits + split) * kAttnRows) + i;
-      a.ws_ml[2 * wrow] = -INFINITY;
-      a.ws_ml[2 * wrow + 1] = 0.f;
+      if (in_bounds((long long)wrow, (long long)a.B * a.Hkv * a.tiles * a.splits * kAttnRows, a.status)) {
+        a.ws_ml[2 * wrow] = -INFINITY;
+        a.ws_ml[2 * wrow + 1] = 0.f;
+      }
     }
   }
 
@@ -501,6 +507,10 @@ __global__ void __launch_bounds__(256) tree_attention_combine_kernel(AttnArgs a)
   }
   if (__any_sync(0xffffffffu, bad)) return;
   const size_t row0 = (((size_t(r) * a.Hkv + g) * a.tiles + tile) * a.splits) * kAttnRows + i;
+  if (!in_bounds((long long)(row0 + size_t(a.splits - 1) * kAttnRows),
+                 (long long)a.B * a.Hkv * a.tiles * a.splits * kAttnRows, a.status) ||
+      !in_bounds((long long)(t0 + t) * a.Hq + g * a.G + (i % a.G), (long long)a.T * a.Hq, a.status))
+    return;
   float M = -INFINITY;
   for (int s = 0; s < a.splits; ++s) M = fmaxf(M, a.ws_ml[2 * (row0 + size_t(s) * kAttnRows)]);
   constexpr int PER = D / 32;

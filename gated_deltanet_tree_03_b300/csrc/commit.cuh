@@ -14,6 +14,7 @@
 // traffic: one read and one write per element, nothing else.
 #pragma once
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -59,7 +60,9 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving 
     if (si == kBadSlot && tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_SLOT);
     return;
   }
-  float *ST = a.ST + (SV ? size_t(si) * a.H + h : size_t(pair)) * DK * DV;
+  const size_t st_off = (SV ? size_t(si) * a.H + h : size_t(pair)) * DK * DV;
+  if (!range_in_bounds((long long)st_off, DK * DV, state_count<SV>(sv, a.B) * a.H * DK * DV, a.status)) return;
+  float *ST = a.ST + st_off;
   const int HK = a.H / qk_group<SV>(sv), hk = h / qk_group<SV>(sv);  // q/k heads, this value head's q/k head
 
   if (tid == 0) {
@@ -94,7 +97,9 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving 
 
   // path check and coefficient staging overlap the state copy
   const int32_t *path_r = a.path + size_t(r) * a.max_path;
-  const bool path_ok = check_path(a.parent, path_r, t0, n, L, a.max_path);
+  // a checked path names nodes 0 <= x < n, so every row t0 + x below lies inside [0, T)
+  const bool path_ok = check_path(a.parent, path_r, t0, n, L, a.max_path) &&
+                       range_in_bounds(t0, n, a.T, a.status);
   if (path_ok) {
     const int l = path_r[L - 1];
     const float Gl = a.G[size_t(t0 + l) * a.H + h];

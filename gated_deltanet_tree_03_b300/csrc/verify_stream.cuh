@@ -23,6 +23,7 @@
 // and write every state element once between them instead of reading it twice.
 #pragma once
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "verify_simt.cuh"
 
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     return;
   }
   const size_t st_off = (SV ? size_t(si) * a.H + h : size_t(pair)) * DK * DV;
+  if (!range_in_bounds((long long)st_off, DK * DV, state_count<SV>(sv, a.B) * a.H * DK * DV, a.status)) return;
   const float2 *st = reinterpret_cast<const float2 *>(a.ST + st_off) + col2;
 
   // 1) the first state rows go out before any dependent load
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
   const int t0 = a.cu_nodes[r];
   const int n = a.cu_nodes[r + 1] - t0;
   bool vok = true;
+  // every node row below is t0 + t with t < n; with offsets_ok that stays inside [0, T)
   if (!offsets_ok(t0, n, a.T)) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_OFFSETS);
     vok = false;
@@ -134,11 +137,14 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
       for (int i = tid; i < L * DK; i += NT) {
         const int q = i / DK, row = i % DK;
         const size_t th = size_t(tp0 + path_r[q]) * H + h;
-        Ws[q][row] = expf(Gl - c.G[th]) * bf16_to_f32(c.k[(size_t(tp0 + path_r[q]) * HK + hk) * DK + row]);
+        Ws[q][row] = in_bounds(tp0 + path_r[q], c.T, a.status)
+                         ? expf(Gl - c.G[th]) * bf16_to_f32(c.k[(size_t(tp0 + path_r[q]) * HK + hk) * DK + row])
+                         : 0.f;
       }
 #pragma unroll
       for (int q = 0; q < LW; ++q)
-        if (q < L) us[q] = reinterpret_cast<const float2 *>(c.U + (size_t(tp0 + path_r[q]) * H + h) * DV)[col2];
+        if (q < L && in_bounds(tp0 + path_r[q], c.T, a.status))
+          us[q] = reinterpret_cast<const float2 *>(c.U + (size_t(tp0 + path_r[q]) * H + h) * DV)[col2];
       Lc = L;
     }
   }
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
     const int row = i / (DK / 4), c4 = i % (DK / 4);
     const int t = row < NMAX ? row : row - NMAX;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < n) {
+    if (t < n && in_bounds(t0 + t, a.T, a.status)) {
       const uint16_t *src = (row < NMAX ? a.k : a.q) + (size_t(t0 + t) * HK + hk) * DK + 4 * c4;
       const uint2 w = *reinterpret_cast<const uint2 *>(src);
       const float2 lo = bf16x2_to_f32(w.x), hi = bf16x2_to_f32(w.y);
@@ -160,9 +166,9 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
   uint32_t vb[NMAX];
 #pragma unroll
   for (int t = 0; t < NMAX; ++t)
-    vb[t] = vok && t < n ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
+    vb[t] = vok && t < n && in_bounds(t0 + t, a.T, a.status) ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
   int bad = 0;
-  if (vok && tid < n) {
+  if (vok && tid < n && in_bounds(t0 + tid, a.T, a.status)) {
     const int p = a.parent[t0 + tid];
     bad = (p < -1 || p >= tid);
     par_s[tid] = p;
@@ -315,11 +321,14 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
       }
       const size_t row = (size_t(t0 + t) * H + h) * DV2 + col2;
       const float qsc = query_scale<SV>(sv);  // o is linear in q
-      __stcs(reinterpret_cast<float2 *>(a.o) + row, make_float2(qsc * o.x, qsc * o.y));
-      __stcs(reinterpret_cast<float2 *>(a.U) + row, u[t]);
+      if (in_bounds((long long)row, (long long)a.T * H * DV2, a.status)) {
+        __stcs(reinterpret_cast<float2 *>(a.o) + row, make_float2(qsc * o.x, qsc * o.y));
+        __stcs(reinterpret_cast<float2 *>(a.U) + row, u[t]);
+      }
     }
   }
-  if (tid < n) a.G[size_t(t0 + tid) * H + h] = G_s[tid];
+  if (tid < n && in_bounds((long long)(t0 + tid) * H + h, (long long)a.T * H, a.status))
+    a.G[size_t(t0 + tid) * H + h] = G_s[tid];
 }
 
 }  // namespace gdn

@@ -47,6 +47,7 @@
 // copies and MMAs in flight, frees its tensor memory and returns.
 #pragma once
 
+#include "bounds.cuh"
 #include "common.cuh"
 #include "ptx.cuh"
 #include "verify_simt.cuh"
@@ -266,6 +267,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int t0, n, si;
         if (!tc_pair_nodes<SV>(a, sv, p, t0, n, si)) continue;
         const size_t st_idx = SV ? size_t(si) * a.H + p % a.H : size_t(p);
+        // (a skipped state leaves its slots unfilled: the pair's waits time out and report it)
+        if (!range_in_bounds((long long)(st_idx * DK * DV), DK * DV, state_count<SV>(sv, a.B) * a.H * DK * DV,
+                             a.status))
+          break;
         const uint8_t *src = reinterpret_cast<const uint8_t *>(a.ST + st_idx * DK * DV);
         bool ok = true;
         for (int c = 0; c < NCHUNK; ++c, ++u) {
@@ -387,11 +392,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int tA = lane, tB = lane + 32;
       int prA = 0, prB = 0;
       float gA = 0.f, gB = 0.f, bA = 0.f, bB = 0.f;
-      if (tA < n) {
+      if (tA < n && in_bounds(t0 + tA, a.T, a.status)) {
         prA = a.parent[t0 + tA];
         gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tA) * a.H + h, h, gA, bA);
       }
-      if (tB < n) {
+      if (tB < n && in_bounds(t0 + tB, a.T, a.status)) {
         prB = a.parent[t0 + tB];
         gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tB) * a.H + h, h, gB, bB);
       }
@@ -719,7 +724,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float *up = u_col + size_t(c0) * node_stride;
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            if (c0 + jj < n) {
+            if (c0 + jj < n && in_bounds(op - a.o, (long long)a.T * a.H * DV, a.status)) {
               const float ov = fmaf(g8[jj], __uint_as_float(x[16 + jj]), __uint_as_float(x[8 + jj]));
               __stcs(op, SV ? qsc * ov : ov);
               __stcs(up, __uint_as_float(x[jj]));
@@ -729,7 +734,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (live && ot < n) a.G[size_t(t0 + ot) * a.H + h] = ts.G[ot];
+      if (live && ot < n && in_bounds((long long)(t0 + ot) * a.H + h, (long long)a.T * a.H, a.status))
+        a.G[size_t(t0 + ot) * a.H + h] = ts.G[ot];
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {

@@ -84,6 +84,8 @@ typedef enum gdn_status {
 #define GDN_STATUS_PATH_TRUNCATED 32u /* an accepted path was longer than max_path            */
 #define GDN_STATUS_BAD_SLOT 64u      /* a state slot outside [0, n_slots) and not -1         */
 #define GDN_STATUS_BAD_PROB 128u     /* an estimated probability outside [0, 1] or NaN        */
+#define GDN_STATUS_OUT_OF_BOUNDS 256u /* debug build only: a computed index fell outside its   */
+                                      /* array; that access was skipped                       */
 
 /*
  * gdn_layout - serving layout of the *_ex entry points: how an inference engine that hosts
