@@ -36,8 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = "draft-node verifications/sec (verify+commit) and achieved HBM GB/s vs B300 peak"
 UNIT = "node-verifications/s"
 KERNEL_SOURCES = {
-    "verify": ["verify_stream.cuh", "verify_tc.cuh", "verify_simt.cuh", "common.cuh", "ptx.cuh"],
-    "commit": ["commit.cuh", "common.cuh", "ptx.cuh"],
+    "verify": ["verify_stream.cuh", "verify_tc.cuh", "verify_simt.cuh", "common.cuh", "ptx.cuh", "bounds.cuh"],
+    "commit": ["commit.cuh", "common.cuh", "ptx.cuh", "bounds.cuh"],
 }
 NOMINAL_HBM_GBS = 8000.0  # the B300 HBM3e figure the roofline target is quoted against
 
