@@ -453,8 +453,14 @@ int attn_sms() {
   return n > 0 ? n : 148;
 }
 
-// Query tiles per (request, head) and key splits: split the prefix only when the (request,
-// head, tile) grid is smaller than two CTAs per SM, and only as far as `ws_limit` bytes allow.
+// Query tiles per (request, head) and key splits. The attention kernel holds one CTA per SM, so
+// a grid of n CTAs runs in ceil(n / SMs) waves, each as long as its slowest CTA. A CTA costs its
+// key blocks plus about one block of fixed work (query load, pipeline fill); a split CTA also
+// writes a partial tile (about one key block of bytes), and the combine pass reads all partials
+// back (two block-equivalents per partial, spread over the SMs). The planner takes the split
+// count with the least estimated time, the fewest splits on a tie, with at most 4 CTAs per SM in
+// total and no more workspace than `ws_limit` bytes. With 4096-key prefixes this keeps grids of
+// 128 and 256 (request, head, tile) CTAs unsplit, where splitting them measured slower.
 AttnPlan attn_plan(int B, int Hq, int Hkv, int d, int max_nodes, int max_prefix, size_t ws_limit) {
   AttnPlan p;
   p.G = Hq / Hkv;
@@ -462,12 +468,20 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int d, int max_nodes, int max_prefix,
   if (p.tiles < 1) p.tiles = 1;
   const long long base = (long long)B * Hkv * p.tiles;
   const int nblk = (max_prefix + kAttnKeys - 1) / kAttnKeys;
-  const int target = 2 * attn_sms();
-  int splits = 1;
-  if (base < target && nblk > 1) splits = int(std::min<long long>(nblk, (target + base - 1) / base));
+  const long long sms = attn_sms();
   const size_t per_split = size_t(base) * kAttnRows * size_t(d + 2) * 4;
-  if (splits > 1 && per_split * splits > ws_limit) splits = int(ws_limit / per_split);
-  if (splits < 2) splits = 1;
+  auto cost = [&](int s) {
+    const int bps = (nblk + s - 1) / s;
+    const long long ctas = base * s;
+    const double waves = double((ctas + sms - 1) / sms);
+    return s == 1 ? waves * (bps + 1.0) : waves * (bps + 2.0) + 2.0 * double(ctas) / double(sms);
+  };
+  int splits = 1;
+  double best = cost(1);
+  for (int s = 2; s <= nblk && base * s <= 4 * sms && per_split * size_t(s) <= ws_limit; ++s) {
+    const double c = cost(s);
+    if (c < best) best = c, splits = s;
+  }
   const int bps = nblk > 0 ? (nblk + splits - 1) / splits : 1;
   p.splits = nblk > 0 ? (nblk + bps - 1) / bps : 1;
   p.blocks_per_split = bps;

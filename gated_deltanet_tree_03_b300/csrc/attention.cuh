@@ -10,13 +10,14 @@
 // keys (128 prefix keys, or the request's <= 64 draft nodes as the last block):
 //     S = Q K^T        tcgen05.mma into tensor memory (two S buffers, so the next block's
 //                      scores are computed while this block's softmax runs)
-//     softmax          one thread per query row: mask (prefix length / ancestor bits), running
+//     softmax          one thread per query row, its scores read once from tensor memory into
+//                      registers: mask (prefix length / ancestor bits), running
 //                      max and sum in the log2 domain, O rescaled in tensor memory when the max
 //                      grows, probabilities written back as bf16 over the S columns they came from
 //     O += P V         tcgen05.mma with P read from tensor memory and V read as an MN-major
 //                      operand straight from its TMA tile
-// Warp roles: 0 key (and query) TMA producer, 1 MMA issuer (issues whichever of the next S and
-// the next P.V is ready), 2 tree masks, 3 value TMA producer, 4..11 softmax and epilogue in two
+// Warp roles: 0 key (and query) TMA producer, 1 MMA issuer (S_0, S_1, then P.V_j and S_{j+2} in
+// turn, each after a blocking wait), 2 tree masks, 3 value TMA producer, 4..11 softmax and epilogue in two
 // warpgroups: warps 4..7 take key columns 0..63 of every block, warps 8..11 columns 64..127,
 // each half with its own running max and sum and its own O accumulator in tensor memory; the
 // two halves are merged once, in the epilogue.
@@ -241,75 +242,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const uint32_t q_addr = ptx::smem_u32(Qs);
       bool ok = attn_wait(&sh.q_full, 0, sh, a.status);
-      // polls both streams: S_j needs its key block and a free S buffer - block j - 2's P.V, which
-      // reads its probabilities from that buffer, issued before it (one thread's MMAs run in
-      // order); P.V_j needs block j's probabilities and its value block
+      // S_j = Q K_j^T into S buffer j & 1, once key block j has landed
+      auto issue_s = [&](int j) {
+        const int sk = j % kAttnKStages;
+        if (!attn_wait(&sh.k_full[sk], (j / kAttnKStages) & 1, sh, a.status)) return false;
+        ptx::tc_fence_after_sync();
+        const bool tree = j == nbp;
+        const uint32_t idesc = ptx::idesc_bf16_f32(kAttnRows, tree ? kAttnTreeKeys : kAttnKeys);
+        const uint32_t k_addr = ptx::smem_u32(Ks + sk * kKVBytes);
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::mma_bf16_ss(tmem + uint32_t(j & 1) * kAttnKeys, ptx::desc_kmajor_sw128(q_addr + c * kChunk + kk * 32),
+                             ptx::desc_kmajor_sw128(k_addr + c * kChunk + kk * 32), idesc, (c | kk) != 0);
+        ptx::mma_commit(&sh.s_full[j & 1]);
+        ptx::mma_commit(&sh.k_empty[sk]);
+        return true;
+      };
+      // Fixed issue order S_0, S_1, then P.V_j followed by S_{j+2}: S_{j+2} overwrites the buffer
+      // whose probabilities P.V_j reads, and one thread's MMAs run in issue order. Every wait
+      // blocks (the thread sleeps in the barrier), so this warp takes no issue slots from the
+      // softmax warps that share its scheduler.
       int si = 0, pi = 0;
       bool o1_started = false;  // half 1's O has had its first (overwriting) P.V
-      uint32_t idle = 0;
-      uint64_t idle_since = 0;
-      while (ok && pi < nb) {
-        bool progress = false;
+      for (; ok && si < nb && si < 2; ++si) ok = issue_s(si);
+      for (; ok && pi < nb; ++pi) {
+        const int sv = pi % kAttnVStages;
+        if (!attn_wait(&sh.p_full[pi & 1], (pi >> 1) & 1, sh, a.status) ||
+            !attn_wait(&sh.v_full[sv], (pi / kAttnVStages) & 1, sh, a.status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after_sync();
+        // one MMA per 16 keys covers all D value columns: the value tile's 64-column chunks are
+        // the operand's atoms along N, kChunk bytes apart
+        const uint32_t idesc = ptx::idesc_bf16_f32_bmn(kAttnRows, D);
+        const uint32_t v_addr = ptx::smem_u32(Vs + sv * kKVBytes);
+        const uint32_t p_tmem = tmem + uint32_t(pi & 1) * kAttnKeys;
+        // half h: keys 64 h .. 64 h + 63, whose P that half wrote (packed, 16 keys = 8 columns) at
+        // columns 64 h .. 64 h + 31 of the buffer, into O of half h; the draft-node block has keys
+        // for half 0 only
+        const int halves = pi == nbp ? 1 : 2;
+        for (int h2 = 0; h2 < halves; ++h2) {
+          for (int kq = 0; kq < 4; ++kq) {
+            const int ks = h2 * 4 + kq;
+            const uint32_t acc = h2 == 0 ? uint32_t((pi | kq) != 0) : uint32_t(o1_started || kq != 0);
+            ptx::mma_bf16_ts(tmem + O_col + uint32_t(h2 * D), p_tmem + uint32_t(h2 * 64 + kq * 8),
+                             ptx::desc_mnmajor_sw128(v_addr + ks * 2048, kChunk), idesc, acc);
+          }
+          if (h2 == 1) o1_started = true;
+        }
+        ptx::mma_commit(&sh.pv_done);
+        ptx::mma_commit(&sh.v_empty[sv]);
         if (si < nb) {
-          const int sk = si % kAttnKStages;
-          if (si <= pi + 1 && ptx::mbar_test_wait(&sh.k_full[sk], (si / kAttnKStages) & 1)) {
-            ptx::tc_fence_after_sync();
-            const bool tree = si == nbp;
-            const uint32_t idesc = ptx::idesc_bf16_f32(kAttnRows, tree ? kAttnTreeKeys : kAttnKeys);
-            const uint32_t k_addr = ptx::smem_u32(Ks + sk * kKVBytes);
-#pragma unroll
-            for (int c = 0; c < NCH; ++c)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_bf16_ss(tmem + uint32_t(si & 1) * kAttnKeys,
-                                 ptx::desc_kmajor_sw128(q_addr + c * kChunk + kk * 32),
-                                 ptx::desc_kmajor_sw128(k_addr + c * kChunk + kk * 32), idesc, (c | kk) != 0);
-            ptx::mma_commit(&sh.s_full[si & 1]);
-            ptx::mma_commit(&sh.k_empty[sk]);
-            ++si;
-            progress = true;
-          }
-        }
-        if (pi < si) {
-          const int sv = pi % kAttnVStages;
-          if (ptx::mbar_test_wait(&sh.p_full[pi & 1], (pi >> 1) & 1) &&
-              ptx::mbar_test_wait(&sh.v_full[sv], (pi / kAttnVStages) & 1)) {
-            ptx::tc_fence_after_sync();
-            const uint32_t idesc = ptx::idesc_bf16_f32_bmn(kAttnRows, 64);
-            const uint32_t v_addr = ptx::smem_u32(Vs + sv * kKVBytes);
-            const uint32_t p_tmem = tmem + uint32_t(pi & 1) * kAttnKeys;
-            // half h: keys 64 h .. 64 h + 63, whose P that half wrote (packed, 16 keys = 8 columns)
-            // at columns 64 h .. 64 h + 31 of the buffer, into O of half h; the draft-node block
-            // has keys for half 0 only
-            const int halves = pi == nbp ? 1 : 2;
-            for (int h2 = 0; h2 < halves; ++h2) {
-              for (int kq = 0; kq < 4; ++kq) {
-                const int ks = h2 * 4 + kq;
-                const uint32_t acc = h2 == 0 ? uint32_t((pi | kq) != 0) : uint32_t(o1_started || kq != 0);
-#pragma unroll
-                for (int c = 0; c < NCH; ++c)
-                  ptx::mma_bf16_ts(tmem + O_col + uint32_t(h2 * D + c * 64), p_tmem + uint32_t(h2 * 64 + kq * 8),
-                                   ptx::desc_mnmajor_sw128(v_addr + c * kChunk + ks * 2048), idesc, acc);
-              }
-              if (h2 == 1) o1_started = true;
-            }
-            ptx::mma_commit(&sh.pv_done);
-            ptx::mma_commit(&sh.v_empty[sv]);
-            ++pi;
-            progress = true;
-          }
-        }
-        if (progress) {
-          idle = 0;
-        } else if ((++idle & 63u) == 0) {  // bounded: give up after the wait limit without progress
-          if (*reinterpret_cast<volatile int *>(&sh.abort_flag)) break;
-          const uint64_t now = ptx::globaltimer_ns();
-          if (idle == 64) idle_since = now;
-          else if (now - idle_since > kAttnWaitNs) {
-            *reinterpret_cast<volatile int *>(&sh.abort_flag) = 1;
-            report(a.status, GDN_STATUS_TIMEOUT);
-            break;
-          }
+          ok = issue_s(si);
+          ++si;
         }
       }
       // O is final once every P.V has completed (the epilogue waits on this single phase: the
@@ -359,15 +347,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         };
         const uint32_t s_addr = tmem + lane_addr + uint32_t(j & 1) * kAttnKeys + uint32_t(hf * 64);
-        // pass 1: block max of the raw scores (the scale is positive: the scaled max is the max scaled)
+        // the row's 64 scores of this half, read once and kept in registers; block max of the raw
+        // scores (the scale is positive: the scaled max is the max scaled)
+        float x[64];
+        ptx::tmem_ld_32x32b_x64(s_addr, x);
+        masked(x);
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        {
-          float x[64];
-          ptx::tmem_ld_32x32b_x64(s_addr, x);
-          masked(x);
 #pragma unroll
-          for (int e = 0; e < 64; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
-        }
+        for (int e = 0; e < 64; ++e) mx[e & 3] = fmaxf(mx[e & 3], x[e]);
         const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
         const float m_new = bmax > m + kAttnRescale ? bmax : m;  // the reference max moves only by > 2^8
         const float alpha = m_new == m ? 1.f : exp2f(m - m_new);
@@ -383,23 +370,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ptx::tc_fence_after_sync();
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 16) {
-            float x[16];
-            ptx::tmem_ld_32x32b_x16(o_addr + uint32_t(c0), x);
+            float y[16];
+            ptx::tmem_ld_32x32b_x16(o_addr + uint32_t(c0), y);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] *= alpha;
-            ptx::tmem_st_32x32b_x16(o_addr + uint32_t(c0), x);
+            for (int e = 0; e < 16; ++e) y[e] *= alpha;
+            ptx::tmem_st_32x32b_x16(o_addr + uint32_t(c0), y);
           }
         }
-        // pass 2: probabilities p = 2^(scale s - m), rounded to bf16 and written back over the
-        // first 32 columns of this half's scores (already read), two keys per 32-bit column.
-        // Their sum is taken before rounding (each rounded weight is within 2^-8 of its exact
-        // value, the same bound as rounding the sum).
+        // probabilities p = 2^(scale s - m), rounded to bf16 and written back over the first 32
+        // columns of this half's scores (already read), two keys per 32-bit column. Their sum is
+        // taken before rounding (each rounded weight is within 2^-8 of its exact value, the same
+        // bound as rounding the sum).
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
         const float sl = a.scale_log2;
         {
-          float x[64];
-          ptx::tmem_ld_32x32b_x64(s_addr, x);
-          masked(x);
           uint32_t w[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {

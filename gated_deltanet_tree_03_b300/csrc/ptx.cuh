@@ -287,14 +287,16 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
 
 // Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzle layout, as a TMA
 // copy with 128-byte swizzle lays out rows of 64 bf16 along N, one row per K index: 8 K-rows x
-// 128 bytes per 1024-byte atom, atoms 1024 bytes apart along K. Used with N = 64 (one atom along
-// N), so the stride between atoms along N never enters; both offset fields hold the K stride.
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr) {
-  return uint64_t((saddr & 0x3FFFFu) >> 4)  // start address, 16-byte units
-         | (uint64_t(1024 >> 4) << 16)      // leading byte offset
-         | (uint64_t(1024 >> 4) << 32)      // stride byte offset
-         | (uint64_t(1) << 46)              // descriptor version for sm_100-class
-         | (uint64_t(2) << 61);             // 128-byte swizzle
+// 128 bytes per 1024-byte atom, atoms 1024 bytes apart along K (the stride byte offset). For an
+// operand wider than 64 along N, `n_atom_bytes` is the distance between consecutive 64-column
+// atoms along N (the leading byte offset, a multiple of 16 below 256 KiB); with N = 64 it never
+// enters.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t n_atom_bytes = 1024u) {
+  return uint64_t((saddr & 0x3FFFFu) >> 4)           // start address, 16-byte units
+         | (uint64_t((n_atom_bytes >> 4) & 0x3FFFu) << 16)  // leading byte offset: next atom along N
+         | (uint64_t(1024 >> 4) << 32)               // stride byte offset: next 8 K-rows
+         | (uint64_t(1) << 46)                       // descriptor version for sm_100-class
+         | (uint64_t(2) << 61);                      // 128-byte swizzle
 }
 
 // Instruction descriptor, kind::f16: A = B = bf16, D = f32, both K-major, shape M x N.

@@ -189,8 +189,8 @@ def test_attention_workspace_size_is_zero_without_splits():
 
 
 def test_attention_workspace_stays_under_its_bound():
-    """The key splits aim at two CTAs per SM, so the workspace stays under 4 x SMs x 128 rows x
-    (d + 2) floats: with the host's SM count unknown here, the planner assumes 148 SMs."""
+    """The key splits never plan more than 4 CTAs per SM, so the workspace stays under 4 x SMs x
+    128 rows x (d + 2) floats: with the host's SM count unknown here, the planner assumes 148 SMs."""
     bound = lambda d: 4 * 148 * 128 * (d + 2) * 4
     for B in (1, 2, 5, 17, 64, 150, 300):
         for Hq, Hkv in ((16, 2), (8, 8), (32, 4), (4, 1)):

@@ -9,7 +9,8 @@ The GPU tests call it through the C ABI:
     same split plan, so any partial write or stale read of the shared scratch shows. One call
     is also compared with the fp64 attention oracle (2^-8 max|v|, the bf16-probability bound);
   * on a shape whose full split plan needs more than the 32 MiB scratch: it runs with the plan
-    that fits (here: no split) and equals gdn_tree_attention given no workspace;
+    that fits, equals bit for bit gdn_tree_attention given a 32 MiB workspace (the same plan),
+    and agrees with the unsplit call within the bf16-probability bound;
   * once more in a fresh Python process, so that the scratch's first use on a device (the
     address lookup) is exercised in a process that has run nothing else.
 The CPU test checks that invalid shapes are refused before anything runs.
@@ -42,7 +43,8 @@ def _i32(x):
 
 def _run(ab, workspace: str):
     """The same inputs through gdn_tree_attention (workspace "full": its own buffer of the planned
-    size; "none": no workspace) and through gdn_tree_attention_noalloc."""
+    size; "scratch": a buffer as large as the built-in scratch; "none": no workspace) and through
+    gdn_tree_attention_noalloc."""
     import torch
     ins = [_bf(ab.q), _bf(ab.k), _bf(ab.v), _bf(ab.k_cache), _bf(ab.v_cache), _i32(ab.cu_prefix), _i32(ab.parent),
            _i32(ab.cu_nodes)]
@@ -51,9 +53,10 @@ def _run(ab, workspace: str):
     o_ref = torch.full((ab.T, ab.Hq, ab.d), float("nan"), device="cuda")
     o_new = torch.full((ab.T, ab.Hq, ab.d), float("nan"), device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
-    if workspace == "full":
-        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        gb.gdn_tree_attention(*ins, *sizes, o_ref, ws, need, st)
+    if workspace in ("full", "scratch"):
+        nb = need if workspace == "full" else SCRATCH_BYTES
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        gb.gdn_tree_attention(*ins, *sizes, o_ref, ws, nb, st)
     else:
         gb.gdn_tree_attention(*ins, *sizes, o_ref, None, 0, st)
     gb.gdn_tree_attention_noalloc(*ins, *sizes, o_new, st)
@@ -94,15 +97,18 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
 
 @pytest.mark.gpu
 def test_noalloc_plans_within_the_scratch():
-    """64 requests x 4096-key prefixes, 16 query / 2 key-value heads, 32-node trees: the full
-    split plan needs about 34 MB. The scratch takes the plan that fits (one split, no scratch)."""
+    """7 requests x 16384-key prefixes, 32 query / 4 key-value heads, 64-node trees: 112 (request,
+    head, tile) CTAs, whose best split plan needs about 37 MB. The scratch takes the best plan that
+    fits in 32 MiB."""
     rng = np.random.default_rng(73)
-    parents = [W.random_tree_parents(rng, 32, 3, 6) for _ in range(64)]
-    ab = W.make_attention_batch(73, B=64, Hq=16, Hkv=2, d=128, prefix_range=(4096, 4096), parents=parents)
-    need, o_ref, o_new = _run(ab, "none")
+    parents = [W.random_tree_parents(rng, 64, 3, 6) for _ in range(7)]
+    ab = W.make_attention_batch(73, B=7, Hq=32, Hkv=4, d=128, prefix_range=(16384, 16384), parents=parents)
+    need, o_ref, o_new = _run(ab, "scratch")
     assert need > SCRATCH_BYTES
     assert np.all(np.isfinite(o_new))
     np.testing.assert_array_equal(o_new, o_ref)
+    _, o_unsplit, _ = _run(ab, "none")
+    assert float(np.max(np.abs(o_new - o_unsplit))) <= _tol(ab)
 
 
 @pytest.mark.gpu
