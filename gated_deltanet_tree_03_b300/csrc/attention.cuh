@@ -126,15 +126,82 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int g = blockIdx.y, r = blockIdx.z;
   const int G = a.G, nodes_per_tile = kAttnRows / G;
 
-  // ---- request checks and the tree's ancestor masks (warp 2), before anything is issued
+  // ---- barriers and tensor memory first, so that the first copies start while warp 2 checks
+  // the request and builds the tree's ancestor masks
   if (tid == 0) {
     sh.go = 0;
     sh.abort_flag = 0;
+    ptx::mbar_init(&sh.q_full, 1);
+    for (int s = 0; s < kAttnKStages; ++s) {
+      ptx::mbar_init(&sh.k_full[s], 1);
+      ptx::mbar_init(&sh.k_empty[s], 1);
+    }
+    for (int s = 0; s < kAttnVStages; ++s) {
+      ptx::mbar_init(&sh.v_full[s], 1);
+      ptx::mbar_init(&sh.v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(&sh.s_full[b], 1);
+    ptx::mbar_init(&sh.p_full[0], 256);
+    ptx::mbar_init(&sh.p_full[1], 256);
+    ptx::mbar_init(&sh.pv_done, 1);
+    ptx::mbar_init(&sh.o_final, 1);
+    ptx::mbar_init(&sh.drain, 1);
+    ptx::fence_mbar_init();
   }
+  if (warp == 1) {
+    ptx::tmem_alloc(&sh.tmem_base, kAttnTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before_sync();
   __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+
   const int t0 = a.cu_nodes[r], n = a.cu_nodes[r + 1] - t0;
   const int p0 = a.cu_prefix[r], P = a.cu_prefix[r + 1] - p0;
   const int t_begin = tile * nodes_per_tile;
+
+  // ---- this split's blocks: prefix blocks [b_lo, b_hi), then the draft-node block (last split)
+  const int n_pre = (P + kAttnKeys - 1) / kAttnKeys;
+  const int b_lo = min(n_pre, split * a.blocks_per_split), b_hi = min(n_pre, b_lo + a.blocks_per_split);
+  const int nbp = b_hi - b_lo;
+  const bool has_tree = split == a.splits - 1;
+  const int nb = nbp + (has_tree ? 1 : 0);
+
+  // TMA producers (lane 0 of warps 0 and 3): block j of keys (warp 0) or values (warp 3) into
+  // stage j % stages. The first `stages` blocks, and the query tile, go out before the request is
+  // checked: with offsets that the checks will reject, their boxes are clipped or filled by the
+  // copy engine (never a fault) and the CTA waits for them before it leaves.
+  const bool producer = (warp == 0 || warp == 3) && lane == 0;
+  const bool keys = warp == 0;
+  const int stages = keys ? kAttnKStages : kAttnVStages;
+  uint64_t *const full = keys ? sh.k_full : sh.v_full;
+  uint64_t *const empty = keys ? sh.k_empty : sh.v_empty;
+  uint8_t *const kvbuf = keys ? Ks : Vs;
+  const CUtensorMap *const pre_map = keys ? &tm_kc : &tm_vc, *const node_map = keys ? &tm_kt : &tm_vt;
+  auto issue_block = [&](int j) {
+    const int st = j % stages;
+    const bool tree = j == nbp;
+    ptx::mbar_arrive_expect_tx(&full[st], tree ? uint32_t(NCH) * kAttnTreeKeys * 128u : kKVBytes);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      if (tree) ptx::tma_load_3d(kvbuf + st * kKVBytes + c * kChunk, node_map, &full[st], c * 64, g, t0);
+      else ptx::tma_load_3d(kvbuf + st * kKVBytes + c * kChunk, pre_map, &full[st], c * 64, g,
+                            p0 + (b_lo + j) * kAttnKeys);
+    }
+  };
+  int issued = 0;  // blocks this producer has issued
+  if (producer && t_begin < n) {  // (a tile without rows leaves at the checks)
+    ptx::prefetch_tensormap(pre_map);
+    if (keys) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::mbar_arrive_expect_tx(&sh.q_full, kQBytes);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) ptx::tma_load_3d(Qs + c * kChunk, &tm_q, &sh.q_full, c * 64, g * G, t0 + t_begin);
+    }
+    for (; issued < stages && issued < nb; ++issued) issue_block(issued);
+  }
+
   if (warp == 2) {
     bool ok = true;
     if (!offsets_ok(t0, n, a.T) || !offsets_ok(p0, P, a.P_total) || P > a.max_prefix) {
@@ -164,73 +231,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   }
   __syncthreads();
-  if (!sh.go) return;  // uniform: nothing issued, nothing allocated
-
-  // ---- this split's blocks: prefix blocks [b_lo, b_hi), then the draft-node block (last split)
-  const int n_pre = (P + kAttnKeys - 1) / kAttnKeys;
-  const int b_lo = min(n_pre, split * a.blocks_per_split), b_hi = min(n_pre, b_lo + a.blocks_per_split);
-  const int nbp = b_hi - b_lo;
-  const bool has_tree = split == a.splits - 1;
-  const int nb = nbp + (has_tree ? 1 : 0);
-
-  if (tid == 0) {
-    ptx::mbar_init(&sh.q_full, 1);
-    for (int s = 0; s < kAttnKStages; ++s) {
-      ptx::mbar_init(&sh.k_full[s], 1);
-      ptx::mbar_init(&sh.k_empty[s], 1);
+  if (!sh.go) {  // uniform: the early copies land and the tensor memory is returned
+    if (producer) {
+      if (keys) ptx::mbar_wait(&sh.q_full, 0, kAttnWaitNs);
+      for (int j = 0; j < issued; ++j) ptx::mbar_wait(&full[j], 0, kAttnWaitNs);
     }
-    for (int s = 0; s < kAttnVStages; ++s) {
-      ptx::mbar_init(&sh.v_full[s], 1);
-      ptx::mbar_init(&sh.v_empty[s], 1);
+    __syncthreads();
+    if (warp == 1) {
+      __syncwarp();
+      ptx::tmem_dealloc(tmem, kAttnTmemCols);
     }
-    for (int b = 0; b < 2; ++b) ptx::mbar_init(&sh.s_full[b], 1);
-    ptx::mbar_init(&sh.p_full[0], 256);
-    ptx::mbar_init(&sh.p_full[1], 256);
-    ptx::mbar_init(&sh.pv_done, 1);
-    ptx::mbar_init(&sh.o_final, 1);
-    ptx::mbar_init(&sh.drain, 1);
-    ptx::fence_mbar_init();
+    return;
   }
-  if (warp == 1) {
-    ptx::tmem_alloc(&sh.tmem_base, kAttnTmemCols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before_sync();
-  __syncthreads();
-  ptx::tc_fence_after_sync();
-  const uint32_t tmem = sh.tmem_base;
   const uint32_t O_col = 2 * kAttnKeys;  // S buffers at columns 0 and 128, then O of half 0, O of half 1
 
   if (warp == 0 || warp == 3) {
     // ---------------------------------------------------------------- TMA producers
     if (lane == 0) {
-      const bool keys = warp == 0;
-      const int stages = keys ? kAttnKStages : kAttnVStages;
-      uint64_t *full = keys ? sh.k_full : sh.v_full;
-      uint64_t *empty = keys ? sh.k_empty : sh.v_empty;
-      uint8_t *buf = keys ? Ks : Vs;
-      const CUtensorMap *pre = keys ? &tm_kc : &tm_vc, *nodes = keys ? &tm_kt : &tm_vt;
-      ptx::prefetch_tensormap(pre);
-      if (keys) {
-        ptx::prefetch_tensormap(&tm_q);
-        ptx::mbar_arrive_expect_tx(&sh.q_full, kQBytes);
-#pragma unroll
-        for (int c = 0; c < NCH; ++c)
-          ptx::tma_load_3d(Qs + c * kChunk, &tm_q, &sh.q_full, c * 64, g * G, t0 + t_begin);
-      }
-      int issued = 0;
-      for (int j = 0; j < nb; ++j) {
-        const int st = j % stages;
-        if (j >= stages && !attn_wait(&empty[st], ((j / stages) - 1) & 1, sh, a.status)) break;
-        const bool tree = j == nbp;
-        ptx::mbar_arrive_expect_tx(&full[st], tree ? uint32_t(NCH) * kAttnTreeKeys * 128u : kKVBytes);
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          if (tree) ptx::tma_load_3d(buf + st * kKVBytes + c * kChunk, nodes, &full[st], c * 64, g, t0);
-          else ptx::tma_load_3d(buf + st * kKVBytes + c * kChunk, pre, &full[st], c * 64, g,
-                                p0 + (b_lo + j) * kAttnKeys);
-        }
-        issued = j + 1;
+      for (; issued < nb; ++issued) {
+        const int j = issued, st = j % stages;
+        if (!attn_wait(&empty[st], ((j / stages) - 1) & 1, sh, a.status)) break;
+        issue_block(j);
       }
       // clean-up: the copies of the last blocks issued have landed before the CTA exits
       if (keys) ptx::mbar_wait(&sh.q_full, 0, kAttnWaitNs);
