@@ -12,8 +12,8 @@
 // the CTA):
 //     R_t = b_t (v_t - gamma_t KS_t),  u_t = R_t - sum_{j strict ancestor} A[t,j] u_j
 //     o_t = gamma_t QS_t + sum_{j ancestor or t} P[t,j] u_j
-// with A[t,j] = b_t exp(G_t - G_j) k_t.k_j and P[t,j] = exp(G_t - G_j) q_t.k_j from warp-split
-// dot products. At N <= 8 the 4 N d_k d_v FMAs per pair stay below the time the pair's state
+// with A[t,j] = b_t exp(G_t - G_j) k_t.k_j and P[t,j] = exp(G_t - G_j) q_t.k_j from one-thread
+// dot products over the staged node block. At N <= 8 the 4 N d_k d_v FMAs per pair stay below the time the pair's state
 // takes to arrive from HBM, so the kernel is bandwidth-bound without tensor cores or any
 // shared-memory round trip of the state.
 //
@@ -60,7 +60,6 @@ template <int DK, int DV, int NMAX, bool FUSE, bool SV>
 __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE))
     verify_stream_kernel(VerifyArgs a, PrevCommit c, Serving sv) {
   constexpr int NT = DV / 2;    // threads
-  constexpr int NW = NT / 32;   // warps
   constexpr int NX = 2 * NMAX;  // node-block rows: keys 0..NMAX-1, queries NMAX..2NMAX-1
   constexpr int DV2 = DV / 2;   // float2 per state row
   constexpr int kStreamPF = stream_prefetch_rows(NMAX);
@@ -73,7 +72,7 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
   __shared__ int par_s[NMAX];
   __shared__ uint32_t anc_s[NMAX];
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int pair = blockIdx.x, h = pair % a.H, r = pair / a.H;
   const int col2 = tid;  // this thread's float2 column index within a state row
   const int si = state_of<SV>(sv, r);  // the request's state (pool slot)
@@ -150,29 +149,44 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
   }
   if (!vok && Lc == 0) return;  // nothing to fold in and nothing to verify
 
-  // 3) node block (fp32, rows >= n zero), this thread's v pairs, tree inputs
-  for (int i = tid; vok && i < NX * DK / 4; i += NT) {
+  // 3) node block (fp32, rows >= n zero), this thread's v pairs, tree inputs: every load goes
+  // out before the first result is used (one memory round trip, not one per staged row)
+  constexpr int NXI = (NX * DK / 4 + NT - 1) / NT;  // node-block words (4 bf16) per thread
+  uint2 xw[NXI];
+#pragma unroll
+  for (int it = 0; it < NXI; ++it) {
+    const int i = tid + it * NT;
     const int row = i / (DK / 4), c4 = i % (DK / 4);
     const int t = row < NMAX ? row : row - NMAX;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < n && in_bounds(t0 + t, a.T, a.status)) {
-      const uint16_t *src = (row < NMAX ? a.k : a.q) + (size_t(t0 + t) * HK + hk) * DK + 4 * c4;
-      const uint2 w = *reinterpret_cast<const uint2 *>(src);
-      const float2 lo = bf16x2_to_f32(w.x), hi = bf16x2_to_f32(w.y);
-      x = make_float4(lo.x, lo.y, hi.x, hi.y);
-    }
-    *reinterpret_cast<float4 *>(&Xs[row][4 * c4]) = x;
+    xw[it] = make_uint2(0u, 0u);
+    if (vok && i < NX * DK / 4 && t < n && in_bounds(t0 + t, a.T, a.status))
+      xw[it] = *reinterpret_cast<const uint2 *>((row < NMAX ? a.k : a.q) + (size_t(t0 + t) * HK + hk) * DK + 4 * c4);
   }
   uint32_t vb[NMAX];
 #pragma unroll
   for (int t = 0; t < NMAX; ++t)
     vb[t] = vok && t < n && in_bounds(t0 + t, a.T, a.status) ? *reinterpret_cast<const uint32_t *>(a.v + (size_t(t0 + t) * H + h) * DV + 2 * col2) : 0u;
+  const bool own = vok && tid < n && in_bounds(t0 + tid, a.T, a.status);  // this thread's node
+  int p_own = -1;
+  float g_own = 0.f, b_own = 0.f;
+  if (own) {
+    p_own = a.parent[t0 + tid];
+    gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tid) * H + h, h, g_own, b_own);
+  }
+#pragma unroll
+  for (int it = 0; it < NXI; ++it) {
+    const int i = tid + it * NT;
+    if (vok && i < NX * DK / 4) {
+      const float2 lo = bf16x2_to_f32(xw[it].x), hi = bf16x2_to_f32(xw[it].y);
+      *reinterpret_cast<float4 *>(&Xs[i / (DK / 4)][4 * (i % (DK / 4))]) = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+  }
   int bad = 0;
-  if (vok && tid < n && in_bounds(t0 + tid, a.T, a.status)) {
-    const int p = a.parent[t0 + tid];
-    bad = (p < -1 || p >= tid);
-    par_s[tid] = p;
-    gate_beta<SV>(sv, a.g, a.beta, size_t(t0 + tid) * H + h, h, g_s[tid], beta_s[tid]);
+  if (own) {
+    bad = (p_own < -1 || p_own >= tid);
+    par_s[tid] = p_own;
+    g_s[tid] = g_own;
+    beta_s[tid] = b_own;
   }
   if (__syncthreads_or(bad)) {
     if (tid == 0 && h == 0) report(a.status, GDN_STATUS_BAD_TREE);
@@ -254,32 +268,32 @@ __global__ void __launch_bounds__(DV / 2) __maxnreg__(stream_max_regs(NMAX, FUSE
 
   if (!vok) return;
 
-  // 5) masked, gated Gram entries: one warp per (t, j) entry, lanes split d_k
+  // 5) masked, gated Gram entries A[t][j] (from k_t.k_j) and P[t][j] (from q_t.k_j) for every j
+  // on t's path: one thread per dot product, straight from shared memory, each thread starting
+  // at its own column so that the float4 reads of a warp spread over the banks
   {
-    int e = 0;
-    for (int t = 0; t < n; ++t) {
-      uint32_t m = anc_s[t];
-      while (m) {
-        const int j = __ffs(m) - 1;
-        m &= m - 1;
-        if (e++ % NW != warp) continue;
-        float kk = 0.f, qk = 0.f;
-#pragma unroll
-        for (int c = lane; c < DK; c += 32) {
-          kk = fmaf(Xs[t][c], Xs[j][c], kk);
-          qk = fmaf(Xs[NMAX + t][c], Xs[j][c], qk);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          kk += __shfl_xor_sync(0xffffffffu, kk, off);
-          qk += __shfl_xor_sync(0xffffffffu, qk, off);
-        }
-        if (lane == 0) {
-          const float w = expf(G_s[t] - G_s[j]);
-          Ac[t][j] = beta_s[t] * w * kk;
-          Pc[t][j] = w * qk;
-        }
+    constexpr int NE = 2 * NMAX * NMAX;
+    for (int e = tid; e < NE; e += NT) {
+      const int kind = e / (NMAX * NMAX), t = (e / NMAX) % NMAX, j = e % NMAX;
+      if (t >= n || !((anc_s[t] >> j) & 1u)) continue;
+      const float *xa = Xs[kind == 0 ? t : NMAX + t];
+      const float *xb = Xs[j];
+      const int rot = (lane * 4) & (DK - 1);
+      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll 8
+      for (int c = 0; c < DK; c += 4) {
+        const int cc = (c + rot) & (DK - 1);
+        const float4 x = *reinterpret_cast<const float4 *>(xa + cc);
+        const float4 y = *reinterpret_cast<const float4 *>(xb + cc);
+        d0 = fmaf(x.x, y.x, d0);
+        d1 = fmaf(x.y, y.y, d1);
+        d2 = fmaf(x.z, y.z, d2);
+        d3 = fmaf(x.w, y.w, d3);
       }
+      const float dot = (d0 + d1) + (d2 + d3);
+      const float w = expf(G_s[t] - G_s[j]);
+      if (kind == 0) Ac[t][j] = beta_s[t] * w * dot;
+      else Pc[t][j] = w * dot;
     }
   }
   __syncthreads();
