@@ -5,13 +5,14 @@
 // With l the accepted path's last node, for every (request, head):
 //   ST[kk][c] <- exp(G_l) ST[kk][c] + sum_{j on path} (exp(G_l - G_j) k_j[kk]) u_j[c]
 //
-// One CTA per (request, head). Thread 0 reads the path length and node offsets and, for a
-// non-empty path, starts one bulk copy (cp.async.bulk, mbarrier completion) of the whole
-// d_k x d_v state into shared memory. While the copy is in flight the CTA checks the path and
-// stages the path's coefficients (exp(G_l - G_j) k_j and u_j). Each thread then owns one fixed
-// group of four state columns, keeps the path's u_j for those columns in registers as it goes,
-// accumulates its float4s and writes each one to HBM once with a streaming store. State
-// traffic: one read and one write per element, nothing else.
+// One CTA per (request, head). Thread 0 first starts the copy of the whole d_k x d_v state into
+// shared memory, as bulk copies (cp.async.bulk) of up to 16 KB, each completing on its own
+// mbarrier; only then does it read the path length and node offsets. While the copies are in
+// flight the CTA checks the path and stages the path's coefficients (exp(G_l - G_j) k_j and
+// u_j). Each thread owns one fixed group of four state columns and, piece by piece as the copies
+// land, accumulates its float4s of that piece and writes each one to HBM once with a streaming
+// store. State traffic: one read and one write per element (an empty or rejected path reads the
+// state and leaves it unchanged).
 #pragma once
 
 #include "bounds.cuh"
@@ -39,17 +40,20 @@ __host__ __device__ inline size_t commit_smem_bytes(int max_path, int dk, int dv
 template <int DK, int DV, bool SV>
 __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving sv) {
   constexpr int DV4 = DV / 4;
-  constexpr int J = DK * DV4 / kThreads;  // float4 of the state per thread
+  constexpr int J = DK * DV4 / kThreads;   // float4 of the state per thread
   constexpr int ROWSTEP = kThreads / DV4;  // state rows between a thread's float4s
   static_assert(J >= 1 && (DK * DV4) % kThreads == 0, "state must tile the block");
   constexpr uint32_t kStateBytes = DK * DV * 4;
-  constexpr uint32_t kPiece = kStateBytes < 16384u ? kStateBytes : 16384u;
+  constexpr int NP = kStateBytes > 16384u ? int(kStateBytes / 16384u) : 1;  // copy pieces
+  constexpr uint32_t kPiece = kStateBytes / NP;
+  constexpr int JP = J / NP;  // a thread's float4s per piece (piece p: j = p JP .. p JP + JP - 1)
+  static_assert(J % NP == 0 && (DK / NP) % ROWSTEP == 0, "pieces must hold whole float4 groups");
 
   extern __shared__ __align__(128) uint8_t commit_dyn[];
   float4 *xs = reinterpret_cast<float4 *>(commit_dyn);
   float *kw = reinterpret_cast<float *>(commit_dyn + kStateBytes);          // [max_path][DK]
   float4 *us = reinterpret_cast<float4 *>(kw + size_t(a.max_path) * DK);  // [max_path][DV4]
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar[NP];
   __shared__ int s_info[3];  // L, t0, n
 
   const int tid = threadIdx.x;
@@ -66,6 +70,15 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving 
   const int HK = a.H / qk_group<SV>(sv), hk = h / qk_group<SV>(sv);  // q/k heads, this value head's q/k head
 
   if (tid == 0) {
+    // the state copy goes out before the dependent loads of the path
+#pragma unroll
+    for (int p = 0; p < NP; ++p) ptx::mbar_init(&bar[p], 1);
+    ptx::fence_mbar_init();
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      ptx::mbar_arrive_expect_tx(&bar[p], kPiece);
+      ptx::bulk_load(commit_dyn + p * kPiece, reinterpret_cast<const uint8_t *>(ST) + p * kPiece, kPiece, &bar[p]);
+    }
     const int L = a.path_len[r];
     const int t0 = a.cu_nodes[r];
     const int n = a.cu_nodes[r + 1] - t0;
@@ -81,24 +94,15 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving 
     s_info[0] = go ? L : 0;
     s_info[1] = t0;
     s_info[2] = n;
-    if (go) {
-      ptx::mbar_init(&bar, 1);
-      ptx::fence_mbar_init();
-      ptx::mbar_arrive_expect_tx(&bar, kStateBytes);
-#pragma unroll
-      for (uint32_t off = 0; off < kStateBytes; off += kPiece)
-        ptx::bulk_load(commit_dyn + off, reinterpret_cast<const uint8_t *>(ST) + off, kPiece, &bar);
-    }
   }
   __syncthreads();
   const int L = s_info[0];
-  if (L == 0) return;  // empty path (keep the state) or a rejected request: no copy in flight
   const int t0 = s_info[1], n = s_info[2];
 
   // path check and coefficient staging overlap the state copy
   const int32_t *path_r = a.path + size_t(r) * a.max_path;
   // a checked path names nodes 0 <= x < n, so every row t0 + x below lies inside [0, T)
-  const bool path_ok = check_path(a.parent, path_r, t0, n, L, a.max_path) &&
+  const bool path_ok = L > 0 && check_path(a.parent, path_r, t0, n, L, a.max_path) &&
                        range_in_bounds(t0, n, a.T, a.status);
   if (path_ok) {
     const int l = path_r[L - 1];
@@ -115,37 +119,44 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitArgs a, Serving 
     }
   }
   __syncthreads();
-  const bool landed = ptx::mbar_wait(&bar, 0, kCommitWaitNs);
-  if (!path_ok || !__syncthreads_and(landed)) {
-    if (tid == 0 && !path_ok && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
-    if (tid == 0 && path_ok) report(a.status, GDN_STATUS_TIMEOUT);
-    if (path_ok) ptx::mbar_wait(&bar, 0, kCommitWaitNs);  // let the copy land before leaving
+  if (!path_ok) {  // empty path (the state stays), or a rejected one: the copies land, nothing is written
+    if (tid == 0 && L > 0 && h == 0) report(a.status, GDN_STATUS_BAD_PATH);
+    if (tid == 0)
+      for (int p = 0; p < NP; ++p) ptx::mbar_wait(&bar[p], 0, kCommitWaitNs);
     return;
   }
 
   const int c4 = tid % DV4, row0 = tid / DV4;
   const float decay = expf(a.G[size_t(t0 + path_r[L - 1]) * a.H + h]);
-  float4 y[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const float4 x = xs[tid + j * kThreads];
-    y[j] = make_float4(decay * x.x, decay * x.y, decay * x.z, decay * x.w);
-  }
-  for (int s = 0; s < L; ++s) {
-    const float4 u = us[s * DV4 + c4];
-    const float *w = kw + s * DK + row0;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const float wv = w[j * ROWSTEP];
-      y[j].x = fmaf(wv, u.x, y[j].x);
-      y[j].y = fmaf(wv, u.y, y[j].y);
-      y[j].z = fmaf(wv, u.z, y[j].z);
-      y[j].w = fmaf(wv, u.w, y[j].w);
-    }
-  }
   float4 *dst = reinterpret_cast<float4 *>(ST);
 #pragma unroll
-  for (int j = 0; j < J; ++j) __stcs(dst + tid + j * kThreads, y[j]);
+  for (int p = 0; p < NP; ++p) {
+    if (!ptx::mbar_wait(&bar[p], 0, kCommitWaitNs)) {  // this piece never landed: nothing more is written
+      if (tid == 0) report(a.status, GDN_STATUS_TIMEOUT);
+      for (int q = p; q < NP; ++q) ptx::mbar_wait(&bar[q], 0, kCommitWaitNs);  // let the copies land before leaving
+      return;
+    }
+    float4 y[JP];
+#pragma unroll
+    for (int jj = 0; jj < JP; ++jj) {
+      const float4 x = xs[tid + (p * JP + jj) * kThreads];
+      y[jj] = make_float4(decay * x.x, decay * x.y, decay * x.z, decay * x.w);
+    }
+    for (int s = 0; s < L; ++s) {
+      const float4 u = us[s * DV4 + c4];
+      const float *w = kw + s * DK + row0 + p * JP * ROWSTEP;
+#pragma unroll
+      for (int jj = 0; jj < JP; ++jj) {
+        const float wv = w[jj * ROWSTEP];
+        y[jj].x = fmaf(wv, u.x, y[jj].x);
+        y[jj].y = fmaf(wv, u.y, y[jj].y);
+        y[jj].z = fmaf(wv, u.z, y[jj].z);
+        y[jj].w = fmaf(wv, u.w, y[jj].w);
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < JP; ++jj) __stcs(dst + tid + (p * JP + jj) * kThreads, y[jj]);
+  }
 }
 
 }  // namespace gdn
