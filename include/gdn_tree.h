@@ -367,10 +367,12 @@ gdn_status gdn_tree_grow_best_first(const float *p_edge, int32_t R, int32_t fano
  *   d                                 64 or 128; H_q / H_kv a power of two <= 128
  *   scale                             score scale, > 0 (e.g. d^-1/2)
  *   o        [T][H_q][d]        fp32  out  written for every node of every valid request
- *   workspace, workspace_bytes        optional device scratch: with too few (request, head)
- *                                     pairs to fill the GPU, long prefixes are split across CTAs
- *                                     and merged, using up to gdn_tree_attention_workspace_size()
- *                                     bytes of it; with NULL or less, fewer splits (none) are made
+ *   workspace, workspace_bytes        optional device scratch: where the (request, head, query
+ *                                     tile) grid fills the GPU's SMs poorly (one CTA per SM: too
+ *                                     few CTAs, or a thin last wave), long prefixes are split
+ *                                     across CTAs and merged, using up to
+ *                                     gdn_tree_attention_workspace_size() bytes of it; with NULL
+ *                                     or less, fewer splits (none) are made
  *   status                            optional: BAD_OFFSETS (offsets outside T / P_total, or a
  *                                     prefix longer than max_prefix), TOO_MANY_NODES, BAD_TREE,
  *                                     TIMEOUT; the request then writes nothing
