@@ -188,6 +188,18 @@ def test_attention_workspace_size_is_zero_without_splits():
     assert big > 0 and big % (128 * 130 * 4) == 0
 
 
+def test_attention_key_splits_follow_the_wave_model():
+    """One CTA per SM: a grid that already fills whole waves stays unsplit, a small one splits.
+    The bench's 4096-key batches (64 requests, 2 key/value heads) have 128 CTAs (6-node trees, one
+    query tile) and 256 (32-node trees, two tiles); splitting either measured slower on B300."""
+    assert gb.gdn_tree_attention_workspace_size(64, 16, 2, 128, 6, 4096) == 0
+    assert gb.gdn_tree_attention_workspace_size(64, 16, 2, 128, 32, 4096) == 0
+    per_tile = 128 * 130 * 4  # one partial tile: 128 rows of (d + 2) floats
+    small = gb.gdn_tree_attention_workspace_size(1, 16, 2, 128, 6, 4096)  # 2 CTAs unsplit
+    assert small > 0 and small % per_tile == 0 and small // per_tile > 2
+    assert small // per_tile <= 148  # the split grid stays within one wave (here 2 x 32 = 64 CTAs)
+
+
 def test_attention_workspace_stays_under_its_bound():
     """The key splits never plan more than 4 CTAs per SM, so the workspace stays under 4 x SMs x
     128 rows x (d + 2) floats: with the host's SM count unknown here, the planner assumes 148 SMs."""
