@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   __syncthreads();
   if (!sh.go) {  // uniform: the early copies land and the tensor memory is returned
-    if (producer) {
+    if (producer && t_begin < n) {  // (the copies went out only for a tile with rows)
       if (keys) ptx::mbar_wait(&sh.q_full, 0, kAttnWaitNs);
       for (int j = 0; j < issued; ++j) ptx::mbar_wait(&full[j], 0, kAttnWaitNs);
     }

@@ -27,7 +27,7 @@ def _run(ab, workspace=True, max_nodes=None, max_prefix=None, parent=None):
     o = torch.full((max(ab.T, 1), ab.Hq, ab.d), float("nan"), device="cuda")
     st = torch.zeros(4, dtype=torch.int32, device="cuda")
     i32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).cuda()
-    ws = None
+    ws, nb = None, 0
     if workspace:
         nb = gb.gdn_tree_attention_workspace_size(ab.B, ab.Hq, ab.Hkv, ab.d, mn, mp)
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
@@ -35,7 +35,7 @@ def _run(ab, workspace=True, max_nodes=None, max_prefix=None, parent=None):
     vc = _bf(ab.v_cache) if ab.P else None
     gb.gdn_tree_attention(_bf(ab.q), _bf(ab.k), _bf(ab.v), kc, vc, i32(ab.cu_prefix),
                           i32(ab.parent if parent is None else parent), i32(ab.cu_nodes), ab.B, ab.Hq, ab.Hkv, ab.T,
-                          ab.P, ab.d, mn, mp, ab.scale, o, ws, 0, st)
+                          ab.P, ab.d, mn, mp, ab.scale, o, ws, nb, st)
     torch.cuda.synchronize()
     return o[:ab.T].cpu().numpy(), int(st[0].item())
 
@@ -119,3 +119,22 @@ def test_bounds_larger_than_the_data():
     assert st1 == 0 and st2 == 0
     _check(ab, o_loose, "loose bounds")
     assert float(np.max(np.abs(o_loose - o_tight))) <= 2.0 ** -8 * 5
+
+
+def test_tiles_without_rows_leave_at_once():
+    """Requests much smaller than the batch's largest leave query tiles without rows (here 16
+    query heads per key/value head: 8 nodes fill a tile, so a 3-node request has two empty tiles
+    out of three). Those CTAs return after their checks; none may wait out the kernel's 1 s
+    bound on a copy it never issued. Also checks the results of such a batch."""
+    import time
+    ab = W.make_attention_batch(91, B=6, Hq=16, Hkv=1, d=128, prefix_range=(200, 900), n_range=(2, 24))
+    assert ab.max_nodes > 16 and int(np.min(np.diff(ab.cu_nodes))) <= 8  # some tiles have no rows
+    o, st = _run(ab)  # warm-up (module load, kernel attributes)
+    assert st == 0
+    t = time.perf_counter()
+    o, st = _run(ab)
+    dt = time.perf_counter() - t
+    assert st == 0
+    assert dt < 0.25, f"{dt:.3f} s for one small call"
+    _check(ab, o, "row-less tiles")
+
