@@ -334,7 +334,7 @@ template <int DK, int DV, bool SV>
 gdn_status launch_commit_sv(const CommitArgs &a, const Serving &L, cudaStream_t stream) {
   const size_t smem = commit_smem_bytes(a.max_path, DK, DV);
   if (ensure_dyn_smem(reinterpret_cast<const void *>(commit_kernel<DK, DV, SV>), smem) != GDN_OK) return GDN_ECUDA;
-  const long long blocks = (long long)a.B * a.H;
+  const long long blocks = (long long)a.B * a.H * commit_row_split(DK, DV);
   commit_kernel<DK, DV, SV><<<unsigned(blocks), kThreads, smem, stream>>>(a, L);
   return launch_status();
 }
@@ -396,7 +396,7 @@ gdn_status commit_impl(float *ST, const float *U, const float *G, const uint16_t
                                     max_path, status);
   if (st != GDN_OK || B == 0) return st;
   if ((st = check_device()) != GDN_OK) return st;
-  if ((long long)B * H > 0x7fffffffLL) return GDN_EINVAL;
+  if ((long long)B * H * 2 > 0x7fffffffLL) return GDN_EINVAL;  // (two CTAs per pair)
   CommitArgs a{ST, U, G, k, parent, cu_nodes, path, path_len, B, H, T, d_k, d_v, max_path, status};
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (d_k * 1000 + d_v) {
